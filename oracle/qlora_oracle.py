@@ -1,0 +1,234 @@
+"""Plain CPU oracle for the fused NF4-QLoRA linear layer (forward and backward).
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports, calls or links
+this module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline
+leg of ``bench.py`` may use it.  It shares no code, table or helper with the
+CUDA library; it keeps its own copy of the NF4 codebook.
+
+What it computes, with the passage each step follows:
+
+* The layer: a frozen base weight W stored in 4-bit NF4, plus a trainable
+  low-rank pair A (d_in x r) and B (r x d_out), scale s, no dropout, no bias:
+  ``Y = X . dequant(W)^T + s . (X . A) . B``.
+  Pages: "UnSloth加速原理：CUDA内核融合与内存优化", section "内核融合" (the
+  Linear -> LoRA_A -> LoRA_B -> Add chain fused into one kernel, and the
+  ``get_peft_model(..., lora_dropout=0, bias="none")`` / ``load_in_4bit``
+  example), and its section "LoRA张量的紧凑布局" (A in R^{d_in x r},
+  B in R^{r x d_out}).  The ReLU that page puts between LoRA_A and LoRA_B is
+  not part of LoRA and is not computed (the LoRA product is linear).
+* The hand-written backward (dX, dA, dB; no gradient for the frozen base):
+  page "解锁 AI 潜能：Unsloth 的算法奥秘与实现全解析", section "Triton 编写的高效内核"
+  (gradients computed by hand), and page "Unsloth性能实测：比传统方法快2倍真的吗？",
+  section 3.2 "框架层：手动反向传播引擎" (LoRA gradients injected directly).
+* The scale: s = alpha / r, or alpha / sqrt(r) for the rank-stabilised variant,
+  page "Unsloth更新日志解读：新功能带来的实际收益", section 2.1 "--use_rslora".
+  The oracle takes s itself.
+* NF4 storage: the pages name NF4 only (page "UnSloth加速原理", section "内核融合",
+  ``load_in_4bit=True``; page "Unsloth更新日志解读", section 1.1, NF4-resident
+  weights).  The concrete format is the plainest reading: the 16-level NF4 code
+  table published with QLoRA (Dettmers et al., 2023, "QLoRA: Efficient
+  Finetuning of Quantized LLMs", Appendix E), blocks of 64 consecutive elements
+  of the row-major weight, one fp32 absmax per block, no second-level
+  quantisation of the absmax, two codes per byte with the first element in the
+  high nibble.
+
+Precision: the NF4 code decision is taken in fp32 (correctly rounded division
+w / absmax, then an exact comparison against the midpoints between adjacent
+codes, evaluated in double where they are exact); dequantisation is one fp32
+multiply rounded to nearest-even bf16.  Those steps decide integers or bits and
+are fixed by the format.  The contractions are evaluated in fp64 from the
+bf16-valued inputs, so the oracle is the exact result up to fp64 rounding.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+# NF4 code table, ascending; QLoRA (Dettmers et al., 2023), Appendix E.
+# Seven negative levels, zero, eight positive levels; c[0] = -1, c[7] = 0, c[15] = 1.
+NF4_CODE = np.array(
+    [
+        -1.0,
+        -0.6961928009986877,
+        -0.5250730514526367,
+        -0.39491748809814453,
+        -0.28444138169288635,
+        -0.18477343022823334,
+        -0.09105003625154495,
+        0.0,
+        0.07958029955625534,
+        0.16093020141124725,
+        0.24611230194568634,
+        0.33791524171829224,
+        0.44070982933044434,
+        0.5626170039176941,
+        0.7229568362236023,
+        1.0,
+    ],
+    dtype=np.float32,
+)
+
+BLOCK = 64          # elements per absmax block (flattened row-major)
+ZERO_CODE = 7       # index of 0.0 in NF4_CODE
+
+
+def bf16_round(x) -> np.ndarray:
+    """Round float32 values to the nearest bf16 (ties to even); return float32.
+
+    bf16 keeps the upper 16 bits of the IEEE binary32 pattern.  Rounding to
+    nearest-even adds 0x7FFF plus the lowest kept bit before truncating.
+    Finite inputs only.
+    """
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    if not np.all(np.isfinite(f)):
+        raise ValueError("bf16_round: non-finite input")
+    u = f.view(np.uint32).astype(np.uint64)
+    lsb = (u >> np.uint64(16)) & np.uint64(1)
+    r = ((u + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)
+    return r.astype(np.uint32).view(np.float32).reshape(f.shape)
+
+
+def bf16_bits(x) -> np.ndarray:
+    """uint16 bit patterns of float32 values that are already bf16-exact."""
+    f = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    u = f.view(np.uint32)
+    if np.any(u & np.uint32(0xFFFF)):
+        raise ValueError("bf16_bits: value is not bf16-representable")
+    return (u >> np.uint32(16)).astype(np.uint16)
+
+
+def code_midpoints() -> np.ndarray:
+    """The 15 decision boundaries (c[i] + c[i+1]) / 2, in double (exact there)."""
+    c = NF4_CODE.astype(np.float64)
+    return (c[:-1] + c[1:]) / 2.0
+
+
+def nearest_code(x32) -> np.ndarray:
+    """Index of the nearest NF4 level to each fp32 value x (ties -> lower index).
+
+    q = number of midpoints strictly below x.  An x exactly on a midpoint is not
+    above it, so it keeps the lower index.
+    """
+    x = np.asarray(x32, dtype=np.float32).astype(np.float64)
+    mids = code_midpoints()
+    q = np.zeros(x.shape, dtype=np.int64)
+    for m in mids:               # 15 comparisons, one per boundary
+        q += (x > m).astype(np.int64)
+    return q.astype(np.uint8)
+
+
+def quantize_nf4(W) -> tuple[np.ndarray, np.ndarray]:
+    """NF4-quantise a bf16-valued weight W [n_out, n_in] (given as float32).
+
+    Returns (packed uint8 [n_out*n_in/2], absmax float32 [n_out*n_in/64]).
+    Per block b of 64 consecutive elements of the row-major flattening:
+    absmax_b = max |w| (exact in fp32); if absmax_b == 0 every code is the zero
+    level; else x = fl32(w / absmax_b) and q = nearest_code(x).  Byte j holds
+    code 2j in its high nibble and code 2j+1 in its low nibble.
+    """
+    W = np.asarray(W, dtype=np.float32)
+    if W.ndim != 2:
+        raise ValueError("W must be 2-D [n_out, n_in]")
+    if W.size % BLOCK != 0:
+        raise ValueError("element count must be a multiple of 64")
+    if not np.all(np.isfinite(W)):
+        raise ValueError("non-finite weights are not supported")
+    flat = W.reshape(-1, BLOCK)
+    absmax = np.max(np.abs(flat), axis=1).astype(np.float32)
+    q = np.full(flat.shape, ZERO_CODE, dtype=np.uint8)
+    nz = absmax > 0
+    if np.any(nz):
+        x = (flat[nz] / absmax[nz][:, None]).astype(np.float32)   # IEEE fp32 division
+        q[nz] = nearest_code(x)
+    q = q.reshape(-1)
+    packed = ((q[0::2] << 4) | q[1::2]).astype(np.uint8)
+    return packed, absmax
+
+
+def unpack_codes(packed) -> np.ndarray:
+    """Codes in element order from the packed stream (high nibble first)."""
+    p = np.asarray(packed, dtype=np.uint8)
+    q = np.empty(p.size * 2, dtype=np.uint8)
+    q[0::2] = p >> 4
+    q[1::2] = p & 0x0F
+    return q
+
+
+def dequantize_nf4(packed, absmax, n_out: int, n_in: int) -> np.ndarray:
+    """W_deq [n_out, n_in] as bf16-exact float32: bf16_rn(fl32(c[q] * absmax_b))."""
+    q = unpack_codes(packed)
+    if q.size != n_out * n_in:
+        raise ValueError("packed size does not match the shape")
+    a = np.asarray(absmax, dtype=np.float32)
+    scale = np.repeat(a, BLOCK)
+    prod = (NF4_CODE[q] * scale).astype(np.float32)      # one fp32 multiply
+    return bf16_round(prod).reshape(n_out, n_in)
+
+
+def _f64(x):
+    """fp64 view of an input: bf16/fp32 values widen exactly; fp64 stays as is
+    (the finite-difference pins perturb inputs in fp64)."""
+    a = np.asarray(x)
+    if a.dtype == np.float64:
+        return a
+    return a.astype(np.float32).astype(np.float64)
+
+
+def lora_forward(X, W_deq, A, B, s: float, rows=None):
+    """Forward pass: returns (Y, T) in fp64.
+
+    T = X . A            (M x r; the activation saved for the backward)
+    Y = X . W_deq^T + s . T . B
+    ``rows`` restricts both outputs to those rows of X (each row of the layer
+    is independent of the others, so this is the same result row by row).
+    """
+    X = _f64(X)
+    if rows is not None:
+        X = X[np.asarray(rows)]
+    Wd, A64, B64 = _f64(W_deq), _f64(A), _f64(B)
+    T = X @ A64
+    Y = X @ Wd.T + float(s) * (T @ B64)
+    return Y, T
+
+
+def lora_backward(X, dY, W_deq, A, B, s: float, T=None, dx_rows=None):
+    """Hand-written backward: returns (dX, dA, dB) in fp64.
+
+    G  = dY . B^T                  (M x r)
+    dX = dY . W_deq + s . G . A^T  (the base weight's forward operand was W_deq^T)
+    dA = s . X^T . G
+    dB = s . T^T . dY,  T = X . A
+    W is frozen: there is no dW.  ``dx_rows`` restricts dX to those rows
+    (dA and dB always reduce over every row).  ``T`` may be passed to reuse
+    the forward's saved activation.
+    """
+    X64, dY64 = _f64(X), _f64(dY)
+    Wd, A64, B64 = _f64(W_deq), _f64(A), _f64(B)
+    s = float(s)
+    if T is None:
+        T = X64 @ A64
+    else:
+        T = np.asarray(T, dtype=np.float64)
+    G = dY64 @ B64.T
+    dA = s * (X64.T @ G)
+    dB = s * (T.T @ dY64)
+    if dx_rows is None:
+        dX = dY64 @ Wd + s * (G @ A64.T)
+    else:
+        r_ = np.asarray(dx_rows)
+        dX = dY64[r_] @ Wd + s * (G[r_] @ A64.T)
+    return dX, dA, dB
+
+
+def merged_weight(W_deq, A, B, s: float) -> np.ndarray:
+    """Merged dense weight W_deq + s . (A . B)^T in fp64 (the 16-bit export).
+
+    Page "这不是“魔法”是把Unsloth的底层优化逻辑榨干了用", section 4
+    (``save_pretrained_merged(..., "merged_16bit")``): the adapter folded
+    into the base weight.
+    """
+    return _f64(W_deq) + float(s) * (_f64(A) @ _f64(B)).T
+
+
+def lora_scale(alpha: float, r: int, rank_stabilised: bool = False) -> float:
+    """s = alpha / r, or alpha / sqrt(r) for the rank-stabilised variant."""
+    return float(alpha) / (float(np.sqrt(r)) if rank_stabilised else float(r))
