@@ -1,0 +1,159 @@
+/*
+ * qlora.h -- C ABI of the fused NF4-QLoRA linear layer for NVIDIA B300 (sm_103a).
+ *
+ * The layer: a frozen base weight W [d_out, d_in] stored in 4-bit NF4, a
+ * trainable low-rank pair A [d_in, r], B [r, d_out], scale s, no dropout, no bias:
+ *
+ *     Y  = X . W_deq^T + s . (X . A) . B
+ *     dX = dY . W_deq + s . (dY . B^T) . A^T
+ *     dA = s . X^T . (dY . B^T)
+ *     dB = s . (X . A)^T . dY          (no gradient for the frozen W)
+ *
+ * Sources on the Unsloth pages:
+ *   - the fused Linear -> LoRA_A -> LoRA_B -> Add chain, "UnSloth加速原理：CUDA内核融合与内存优化",
+ *     section "内核融合" (its ReLU between LoRA_A and LoRA_B is not LoRA and is not computed);
+ *   - A in R^{d_in x r}, B in R^{r x d_out}: same page, section "LoRA张量的紧凑布局";
+ *   - lora_dropout=0, bias="none", load_in_4bit (NF4): same page, section "内核融合";
+ *   - the hand-written backward: "解锁 AI 潜能：Unsloth 的算法奥秘与实现全解析", section
+ *     "Triton 编写的高效内核", and "Unsloth性能实测：比传统方法快2倍真的吗？", section 3.2;
+ *   - s = alpha/r or alpha/sqrt(r) (rank-stabilised): "Unsloth更新日志解读：新功能带来的实际收益",
+ *     section 2.1.  The caller passes s itself.
+ *
+ * NF4 format (the pages name NF4 only; this is the plainest reading): the
+ * 16-level NF4 table of QLoRA (Dettmers et al., 2023, Appendix E); blocks of
+ * 64 consecutive elements of the row-major weight; one fp32 absmax per block
+ * (no second-level quantisation); codes q = nearest level of fl32(w/absmax),
+ * ties to the lower index, all-zero blocks -> code 7 (0.0) and absmax 0; two
+ * codes per byte, FIRST element in the HIGH nibble.  Dequantised value:
+ * bf16_rne(fl32(code[q] * absmax)).
+ *
+ * Conventions for every call:
+ *   - bf16 tensors are passed as `uint16_t*` bit patterns; all tensors are
+ *     dense, row-major, contiguous, in DEVICE memory owned by the caller;
+ *   - every device pointer must be 16-byte aligned (QLORA_ERR_ALIGN);
+ *   - calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream); the library allocates no device memory; scratch comes
+ *     from the caller's `workspace`;
+ *   - argument errors return a non-OK status and launch nothing; a failed
+ *     launch returns QLORA_ERR_CUDA and qlora_last_cuda_error() gives the
+ *     cudaError_t value;
+ *   - every device-side wait is bounded (about one second); a wait that runs
+ *     out records QLORA_ERR_TIMEOUT in a device status word read by
+ *     qlora_device_status(); the kernel then returns without finishing.
+ */
+#ifndef QLORA_H_
+#define QLORA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum qlora_status {
+  QLORA_OK = 0,
+  QLORA_ERR_NULL = 1,         /* a required pointer is NULL */
+  QLORA_ERR_SHAPE = 2,        /* a size is negative, zero where not allowed, or too large */
+  QLORA_ERR_ALIGN = 3,        /* a device pointer is not 16-byte aligned */
+  QLORA_ERR_UNSUPPORTED = 4,  /* d_in % 64 != 0, d_out % 8 != 0, r outside [1, 128] */
+  QLORA_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed; see qlora_last_cuda_error() */
+  QLORA_ERR_TIMEOUT = 6,      /* a bounded device-side wait ran out (see qlora_device_status) */
+  QLORA_ERR_WORKSPACE = 7     /* workspace NULL or smaller than qlora_workspace_bytes() */
+} qlora_status;
+
+struct CUstream_st;
+typedef struct CUstream_st* qlora_stream_t; /* identical to cudaStream_t */
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* qlora_status_string(qlora_status status);
+
+/* cudaError_t value of the most recent failing CUDA call made by this library
+ * on the calling thread (0 if none). */
+int qlora_last_cuda_error(void);
+
+/* Host copy of the 16 NF4 levels the kernels use, ascending (for checks). */
+void qlora_nf4_codebook(float out[16]);
+
+/* Synchronises the current device, then reads the library's device status
+ * word into *code (a qlora_status; QLORA_OK if no kernel recorded an error)
+ * and clears it when `clear` is non-zero.  Returns QLORA_ERR_CUDA if the
+ * synchronisation or the read fails. */
+qlora_status qlora_device_status(int* code, int clear);
+
+/*
+ * NF4 quantisation of a bf16 weight (offline; once per weight).
+ *   W       [n_out, n_in] bf16, read.
+ *   packed  [n_out * n_in / 2] bytes, written (2 codes per byte, high nibble first).
+ *   absmax  [n_out * n_in / 64] fp32, written (block b = elements 64b..64b+63
+ *           of the row-major flattening).
+ * Requires n_out >= 1, n_in >= 64, n_in % 64 == 0.  W must be finite
+ * (non-finite inputs give unspecified codes).  Bit-exact with the format
+ * above: division is IEEE correctly rounded, boundaries are exact midpoints.
+ * Pages: "UnSloth加速原理：CUDA内核融合与内存优化", section "内核融合" (load_in_4bit).
+ */
+qlora_status qlora_quantize_nf4(const uint16_t* W, int64_t n_out, int64_t n_in,
+                                uint8_t* packed, float* absmax, qlora_stream_t stream);
+
+/*
+ * NF4 dequantisation: W_out[i] = bf16_rne(fl32(code[q_i] * absmax[i / 64])).
+ *   packed, absmax as produced by qlora_quantize_nf4 (read);
+ *   W_out  [n_out, n_in] bf16, written.
+ * Requires n_out >= 1, n_in >= 64, n_in % 64 == 0.  Bit-exact.
+ * The fused kernels dequantise with the same per-block table, so their
+ * weight operand equals this output bit for bit.
+ */
+qlora_status qlora_dequant_nf4(const uint8_t* packed, const float* absmax,
+                               int64_t n_out, int64_t n_in, uint16_t* W_out,
+                               qlora_stream_t stream);
+
+/* Bytes of scratch qlora_linear_fwd / qlora_linear_bwd need for this shape
+ * (0 if the shape is unsupported).  The same workspace serves both calls. */
+size_t qlora_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int32_t r);
+
+/*
+ * Forward:  Y = X . W_deq^T + s . T . B,   T = X . A   (T saved for the backward).
+ *   X        [M, d_in]  bf16, read.
+ *   packed, absmax: NF4 weight of shape [d_out, d_in] (qlora_quantize_nf4 layout), read.
+ *   A        [d_in, r]  bf16, read.      B [r, d_out] bf16, read.
+ *   s        LoRA scale (alpha/r or alpha/sqrt(r)).
+ *   Y        [M, d_out] bf16, written (overwritten, never accumulated into).
+ *   XA_save  [M, r]     fp32, written: T, needed by qlora_linear_bwd.
+ *   workspace / workspace_bytes: caller scratch, >= qlora_workspace_bytes().
+ * Requires M >= 0 (M == 0 launches nothing), d_in % 64 == 0, d_out % 8 == 0,
+ * 1 <= r <= 128.  Accuracy: fp32 accumulation of bf16 products; the LoRA term
+ * enters the tensor-core accumulator as bf16(s*T) x B.
+ */
+qlora_status qlora_linear_fwd(const uint16_t* X, int64_t M, int64_t d_in, int64_t d_out,
+                              const uint8_t* packed, const float* absmax,
+                              const uint16_t* A, const uint16_t* B, int32_t r, float s,
+                              uint16_t* Y, float* XA_save,
+                              void* workspace, size_t workspace_bytes,
+                              qlora_stream_t stream);
+
+/*
+ * Backward (the hand-written gradients; W is frozen, so there is no dW):
+ *   G  = dY . B^T
+ *   dX = dY . W_deq + s . G . A^T      [M, d_in]  bf16, written; may be NULL to skip
+ *   dA = s . X^T . G                   [d_in, r]  fp32, written (overwritten)
+ *   dB = s . T^T . dY                  [r, d_out] fp32, written (overwritten)
+ *   X [M, d_in], dY [M, d_out] bf16, read; XA_saved [M, r] fp32 = T from the
+ *   forward, read; packed/absmax/A/B/r/s as in the forward.
+ * M == 0 writes dA = dB = 0.  Reductions over M are deterministic (fixed
+ * order, no atomics on data).  Pages: "Unsloth性能实测：比传统方法快2倍真的吗？",
+ * section 3.2 (LoRA gradients injected directly, no autograd graph).
+ */
+qlora_status qlora_linear_bwd(const uint16_t* X, const uint16_t* dY,
+                              int64_t M, int64_t d_in, int64_t d_out,
+                              const uint8_t* packed, const float* absmax,
+                              const uint16_t* A, const uint16_t* B, int32_t r, float s,
+                              const float* XA_saved,
+                              uint16_t* dX, float* dA, float* dB,
+                              void* workspace, size_t workspace_bytes,
+                              qlora_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLORA_H_ */

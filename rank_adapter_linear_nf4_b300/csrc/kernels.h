@@ -1,0 +1,47 @@
+// kernels.h -- internal launch interface between the C ABI layer and the
+// kernels (not part of the public API).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qlora {
+
+// NF4 codec (nf4_codec.cu).
+cudaError_t launch_quantize_nf4(const uint16_t* W, int64_t n_elems, uint8_t* packed, float* absmax,
+                                cudaStream_t stream);
+cudaError_t launch_dequant_nf4(const uint8_t* packed, const float* absmax, int64_t n_elems,
+                               uint16_t* W_out, cudaStream_t stream);
+void nf4_levels_host(float out[16]);
+
+// LoRA linear (lora_kernels.cu).
+struct LayerDims {
+  int M;       // tokens
+  int K;       // d_in
+  int N;       // d_out
+  int r;       // LoRA rank
+  int rp;      // r padded to a multiple of 64
+  float s;     // LoRA scale
+};
+
+// Workspace carve-up shared by the forward and the backward.
+struct Workspace {
+  uint16_t* a_pad;   // [K, rp]  A with zero columns r..rp-1
+  uint16_t* b_t;     // [N, rp]  B transposed, zero columns r..rp-1
+  uint16_t* s_t;     // [M, rp]  bf16(s * X.A), zero-padded
+  uint16_t* s_g;     // [M, rp]  bf16(s * dY.B^T), zero-padded
+};
+size_t workspace_bytes(const LayerDims& d);
+Workspace carve_workspace(const LayerDims& d, void* base);
+
+cudaError_t run_forward(const LayerDims& d, const uint16_t* X, const uint8_t* packed,
+                        const float* absmax, const uint16_t* A, const uint16_t* B, uint16_t* Y,
+                        float* XA, const Workspace& ws, int* status, cudaStream_t stream);
+
+cudaError_t run_backward(const LayerDims& d, const uint16_t* X, const uint16_t* dY,
+                         const uint8_t* packed, const float* absmax, const uint16_t* A,
+                         const uint16_t* B, const float* XA, uint16_t* dX, float* dA, float* dB,
+                         const Workspace& ws, int* status, cudaStream_t stream);
+
+}  // namespace qlora

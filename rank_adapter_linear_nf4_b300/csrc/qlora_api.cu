@@ -1,0 +1,195 @@
+// qlora_api.cu -- the C ABI (include/qlora.h): argument validation, status
+// codes, the device status word, and launch sequencing on the caller's stream.
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qlora.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+// Device status word: bounded device-side waits that run out write here.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {nullptr};
+
+qlora_status cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return QLORA_ERR_CUDA;
+}
+
+// Device address of the status word for the current device.
+qlora_status status_word(int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return QLORA_ERR_UNSUPPORTED;
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_status);
+    if (e != cudaSuccess) return cuda_fail(e);
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return QLORA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Largest sizes the kernels index with 32-bit coordinates.
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+qlora_status check_codec_shape(int64_t n_out, int64_t n_in) {
+  if (n_out < 1 || n_in < 1) return QLORA_ERR_SHAPE;
+  if (n_in % 64 != 0) return QLORA_ERR_UNSUPPORTED;
+  if (n_out > kMaxDim || n_in > kMaxDim || n_out * n_in / 64 > kMaxDim * 8) return QLORA_ERR_SHAPE;
+  return QLORA_OK;
+}
+
+qlora_status check_layer(int64_t M, int64_t d_in, int64_t d_out, int32_t r) {
+  if (M < 0 || d_in < 1 || d_out < 1) return QLORA_ERR_SHAPE;
+  if (M > kMaxDim || d_in > kMaxDim || d_out > kMaxDim) return QLORA_ERR_SHAPE;
+  if (d_in % 64 != 0 || d_out % 8 != 0 || r < 1 || r > 128) return QLORA_ERR_UNSUPPORTED;
+  return QLORA_OK;
+}
+
+qlora::LayerDims dims_of(int64_t M, int64_t d_in, int64_t d_out, int32_t r, float s) {
+  qlora::LayerDims d;
+  d.M = static_cast<int>(M);
+  d.K = static_cast<int>(d_in);
+  d.N = static_cast<int>(d_out);
+  d.r = r;
+  d.rp = (r + 63) / 64 * 64;
+  d.s = s;
+  return d;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qlora_status_string(qlora_status status) {
+  switch (status) {
+    case QLORA_OK: return "QLORA_OK";
+    case QLORA_ERR_NULL: return "QLORA_ERR_NULL: a required pointer is NULL";
+    case QLORA_ERR_SHAPE: return "QLORA_ERR_SHAPE: invalid or too large size";
+    case QLORA_ERR_ALIGN: return "QLORA_ERR_ALIGN: device pointer not 16-byte aligned";
+    case QLORA_ERR_UNSUPPORTED:
+      return "QLORA_ERR_UNSUPPORTED: need d_in % 64 == 0, d_out % 8 == 0, 1 <= r <= 128";
+    case QLORA_ERR_CUDA: return "QLORA_ERR_CUDA: a CUDA call failed (qlora_last_cuda_error)";
+    case QLORA_ERR_TIMEOUT: return "QLORA_ERR_TIMEOUT: a bounded device wait ran out";
+    case QLORA_ERR_WORKSPACE: return "QLORA_ERR_WORKSPACE: workspace missing or too small";
+  }
+  return "unknown qlora_status";
+}
+
+int qlora_last_cuda_error(void) { return g_last_cuda_error; }
+
+void qlora_nf4_codebook(float out[16]) {
+  if (out != nullptr) qlora::nf4_levels_host(out);
+}
+
+qlora_status qlora_device_status(int* code, int clear) {
+  if (code == nullptr) return QLORA_ERR_NULL;
+  int* word = nullptr;
+  qlora_status st = status_word(&word);
+  if (st != QLORA_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e);
+  int v = 0;
+  e = cudaMemcpy(&v, word, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (clear) {
+    e = cudaMemset(word, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  *code = v;
+  return QLORA_OK;
+}
+
+qlora_status qlora_quantize_nf4(const uint16_t* W, int64_t n_out, int64_t n_in, uint8_t* packed,
+                                float* absmax, qlora_stream_t stream) {
+  qlora_status st = check_codec_shape(n_out, n_in);
+  if (st != QLORA_OK) return st;
+  if (!W || !packed || !absmax) return QLORA_ERR_NULL;
+  if (!aligned16(W) || !aligned16(packed) || !aligned16(absmax)) return QLORA_ERR_ALIGN;
+  cudaError_t e = qlora::launch_quantize_nf4(W, n_out * n_in, packed, absmax,
+                                             reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+qlora_status qlora_dequant_nf4(const uint8_t* packed, const float* absmax, int64_t n_out,
+                               int64_t n_in, uint16_t* W_out, qlora_stream_t stream) {
+  qlora_status st = check_codec_shape(n_out, n_in);
+  if (st != QLORA_OK) return st;
+  if (!packed || !absmax || !W_out) return QLORA_ERR_NULL;
+  if (!aligned16(packed) || !aligned16(absmax) || !aligned16(W_out)) return QLORA_ERR_ALIGN;
+  cudaError_t e = qlora::launch_dequant_nf4(packed, absmax, n_out * n_in, W_out,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+size_t qlora_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int32_t r) {
+  if (check_layer(M, d_in, d_out, r) != QLORA_OK) return 0;
+  return qlora::workspace_bytes(dims_of(M, d_in, d_out, r, 1.0f));
+}
+
+qlora_status qlora_linear_fwd(const uint16_t* X, int64_t M, int64_t d_in, int64_t d_out,
+                              const uint8_t* packed, const float* absmax, const uint16_t* A,
+                              const uint16_t* B, int32_t r, float s, uint16_t* Y, float* XA_save,
+                              void* workspace, size_t workspace_bytes, qlora_stream_t stream) {
+  qlora_status st = check_layer(M, d_in, d_out, r);
+  if (st != QLORA_OK) return st;
+  if (!packed || !absmax || !A || !B) return QLORA_ERR_NULL;
+  if (M == 0) return QLORA_OK;
+  if (!X || !Y || !XA_save) return QLORA_ERR_NULL;
+  if (!aligned16(X) || !aligned16(packed) || !aligned16(absmax) || !aligned16(A) ||
+      !aligned16(B) || !aligned16(Y) || !aligned16(XA_save) || !aligned16(workspace))
+    return QLORA_ERR_ALIGN;
+  const qlora::LayerDims d = dims_of(M, d_in, d_out, r, s);
+  if (workspace == nullptr || workspace_bytes < qlora::workspace_bytes(d)) return QLORA_ERR_WORKSPACE;
+  int* status = nullptr;
+  st = status_word(&status);
+  if (st != QLORA_OK) return st;
+  cudaError_t e = qlora::run_forward(d, X, packed, absmax, A, B, Y, XA_save,
+                                     qlora::carve_workspace(d, workspace), status,
+                                     reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+qlora_status qlora_linear_bwd(const uint16_t* X, const uint16_t* dY, int64_t M, int64_t d_in,
+                              int64_t d_out, const uint8_t* packed, const float* absmax,
+                              const uint16_t* A, const uint16_t* B, int32_t r, float s,
+                              const float* XA_saved, uint16_t* dX, float* dA, float* dB,
+                              void* workspace, size_t workspace_bytes, qlora_stream_t stream) {
+  qlora_status st = check_layer(M, d_in, d_out, r);
+  if (st != QLORA_OK) return st;
+  if (!packed || !absmax || !A || !B || !dA || !dB) return QLORA_ERR_NULL;
+  if (!aligned16(packed) || !aligned16(absmax) || !aligned16(A) || !aligned16(B) ||
+      !aligned16(dA) || !aligned16(dB))
+    return QLORA_ERR_ALIGN;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    // empty sums: dA = dB = 0
+    cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * static_cast<size_t>(d_in) * r, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dB, 0, sizeof(float) * static_cast<size_t>(d_out) * r, cs);
+    return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+  }
+  if (!X || !dY || !XA_saved) return QLORA_ERR_NULL;
+  if (!aligned16(X) || !aligned16(dY) || !aligned16(XA_saved) || !aligned16(workspace) ||
+      (dX != nullptr && !aligned16(dX)))
+    return QLORA_ERR_ALIGN;
+  const qlora::LayerDims d = dims_of(M, d_in, d_out, r, s);
+  if (workspace == nullptr || workspace_bytes < qlora::workspace_bytes(d)) return QLORA_ERR_WORKSPACE;
+  int* status = nullptr;
+  st = status_word(&status);
+  if (st != QLORA_OK) return st;
+  cudaError_t e = qlora::run_backward(d, X, dY, packed, absmax, A, B, XA_saved, dX, dA, dB,
+                                      qlora::carve_workspace(d, workspace), status, cs);
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+}  // extern "C"

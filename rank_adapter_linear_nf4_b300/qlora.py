@@ -1,0 +1,195 @@
+"""Thin Python binding of the C ABI in ``include/qlora.h``.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libqlora_b300.so``.  Tensors are torch CUDA tensors (torch is
+used for device memory and streams); calls are queued on the current torch
+stream of the tensors' device.  There is no CPU fallback: if the library is
+not built, or a tensor is not on a CUDA device, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+QLORA_OK = 0
+STATUS_NAMES = {
+    0: "QLORA_OK", 1: "QLORA_ERR_NULL", 2: "QLORA_ERR_SHAPE", 3: "QLORA_ERR_ALIGN",
+    4: "QLORA_ERR_UNSUPPORTED", 5: "QLORA_ERR_CUDA", 6: "QLORA_ERR_TIMEOUT",
+    7: "QLORA_ERR_WORKSPACE",
+}
+
+_c_void_p, _i64, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+
+_SIGNATURES = {
+    "qlora_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "qlora_last_cuda_error": (ctypes.c_int, []),
+    "qlora_nf4_codebook": (None, [ctypes.POINTER(ctypes.c_float)]),
+    "qlora_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
+    "qlora_quantize_nf4": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
+    "qlora_dequant_nf4": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
+    "qlora_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32]),
+    "qlora_linear_fwd": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p,
+                                        _c_void_p, _c_void_p, _i32, _f32, _c_void_p, _c_void_p,
+                                        _c_void_p, _sz, _c_void_p]),
+    "qlora_linear_bwd": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p,
+                                        _c_void_p, _c_void_p, _c_void_p, _i32, _f32, _c_void_p,
+                                        _c_void_p, _c_void_p, _c_void_p, _c_void_p, _sz,
+                                        _c_void_p]),
+}
+
+_lib = None
+
+
+class QloraError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        detail = ""
+        if status == 5 and _lib is not None:
+            detail = f" (cudaError {_lib.qlora_last_cuda_error()})"
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)}{detail}")
+
+
+def load_library(path: str = LIB_PATH):
+    """Loads the native library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with rank_adapter_linear_nf4_b300.build.build()")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(fn: str, status: int):
+    if status != QLORA_OK:
+        raise QloraError(fn, status)
+
+
+def _dev(t: torch.Tensor, name: str, dtype: torch.dtype) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def qlora_status_string(status: int) -> str:
+    return load_library().qlora_status_string(status).decode()
+
+
+def qlora_nf4_codebook() -> list[float]:
+    buf = (ctypes.c_float * 16)()
+    load_library().qlora_nf4_codebook(buf)
+    return list(buf)
+
+
+def qlora_device_status(clear: bool = True) -> int:
+    """Synchronises the device and returns (optionally clears) the status word."""
+    code = ctypes.c_int(0)
+    _check("qlora_device_status", load_library().qlora_device_status(ctypes.byref(code), int(clear)))
+    return code.value
+
+
+def qlora_workspace_bytes(M: int, d_in: int, d_out: int, r: int) -> int:
+    return int(load_library().qlora_workspace_bytes(M, d_in, d_out, r))
+
+
+def qlora_quantize_nf4(W: torch.Tensor, packed: torch.Tensor | None = None,
+                       absmax: torch.Tensor | None = None):
+    """W [n_out, n_in] bf16 -> (packed uint8 [n_out*n_in/2], absmax fp32 [n_out*n_in/64])."""
+    lib = load_library()
+    n_out, n_in = W.shape
+    if packed is None:
+        packed = torch.empty(n_out * n_in // 2, dtype=torch.uint8, device=W.device)
+    if absmax is None:
+        absmax = torch.empty(n_out * n_in // 64, dtype=torch.float32, device=W.device)
+    _check("qlora_quantize_nf4", lib.qlora_quantize_nf4(
+        _dev(W, "W", torch.bfloat16), n_out, n_in, _dev(packed, "packed", torch.uint8),
+        _dev(absmax, "absmax", torch.float32), _stream(W)))
+    return packed, absmax
+
+
+def qlora_dequant_nf4(packed: torch.Tensor, absmax: torch.Tensor, n_out: int, n_in: int,
+                      out: torch.Tensor | None = None) -> torch.Tensor:
+    lib = load_library()
+    if out is None:
+        out = torch.empty(n_out, n_in, dtype=torch.bfloat16, device=packed.device)
+    _check("qlora_dequant_nf4", lib.qlora_dequant_nf4(
+        _dev(packed, "packed", torch.uint8), _dev(absmax, "absmax", torch.float32), n_out, n_in,
+        _dev(out, "out", torch.bfloat16), _stream(packed)))
+    return out
+
+
+def _workspace(M, d_in, d_out, r, device, workspace):
+    need = qlora_workspace_bytes(M, d_in, d_out, r)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+    return workspace, need
+
+
+def qlora_linear_fwd(X: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor,
+                     A: torch.Tensor, B: torch.Tensor, s: float, *,
+                     Y: torch.Tensor | None = None, XA: torch.Tensor | None = None,
+                     workspace: torch.Tensor | None = None):
+    """Y = X . W_deq^T + s . (X . A) . B.  Returns (Y bf16 [M, d_out], XA fp32 [M, r])."""
+    lib = load_library()
+    M, d_in = X.shape
+    r, d_out = B.shape
+    if A.shape != (d_in, r):
+        raise ValueError(f"A must be [{d_in}, {r}], got {tuple(A.shape)}")
+    if Y is None:
+        Y = torch.empty(M, d_out, dtype=torch.bfloat16, device=X.device)
+    if XA is None:
+        XA = torch.empty(M, r, dtype=torch.float32, device=X.device)
+    workspace, _ = _workspace(M, d_in, d_out, r, X.device, workspace)
+    _check("qlora_linear_fwd", lib.qlora_linear_fwd(
+        _dev(X, "X", torch.bfloat16), M, d_in, d_out, _dev(packed, "packed", torch.uint8),
+        _dev(absmax, "absmax", torch.float32), _dev(A, "A", torch.bfloat16),
+        _dev(B, "B", torch.bfloat16), r, float(s), _dev(Y, "Y", torch.bfloat16),
+        _dev(XA, "XA", torch.float32), _dev(workspace, "workspace", torch.uint8),
+        workspace.numel(), _stream(X)))
+    return Y, XA
+
+
+def qlora_linear_bwd(X: torch.Tensor, dY: torch.Tensor, packed: torch.Tensor,
+                     absmax: torch.Tensor, A: torch.Tensor, B: torch.Tensor, s: float,
+                     XA: torch.Tensor, *, need_dX: bool = True,
+                     dX: torch.Tensor | None = None, dA: torch.Tensor | None = None,
+                     dB: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """Hand-written backward.  Returns (dX bf16 [M, d_in] or None, dA fp32 [d_in, r], dB fp32 [r, d_out])."""
+    lib = load_library()
+    M, d_in = X.shape
+    r, d_out = B.shape
+    if dY.shape != (M, d_out):
+        raise ValueError(f"dY must be [{M}, {d_out}], got {tuple(dY.shape)}")
+    if need_dX and dX is None:
+        dX = torch.empty(M, d_in, dtype=torch.bfloat16, device=X.device)
+    if dA is None:
+        dA = torch.empty(d_in, r, dtype=torch.float32, device=X.device)
+    if dB is None:
+        dB = torch.empty(r, d_out, dtype=torch.float32, device=X.device)
+    workspace, _ = _workspace(M, d_in, d_out, r, X.device, workspace)
+    dx_ptr = _dev(dX, "dX", torch.bfloat16) if dX is not None else None
+    _check("qlora_linear_bwd", lib.qlora_linear_bwd(
+        _dev(X, "X", torch.bfloat16), _dev(dY, "dY", torch.bfloat16), M, d_in, d_out,
+        _dev(packed, "packed", torch.uint8), _dev(absmax, "absmax", torch.float32),
+        _dev(A, "A", torch.bfloat16), _dev(B, "B", torch.bfloat16), r, float(s),
+        _dev(XA, "XA", torch.float32), dx_ptr, _dev(dA, "dA", torch.float32),
+        _dev(dB, "dB", torch.float32), _dev(workspace, "workspace", torch.uint8),
+        workspace.numel(), _stream(X)))
+    return dX, dA, dB

@@ -1,0 +1,109 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/qlora.h declares, validates arguments before touching
+the device, and carries the same NF4 table as the oracle."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle import qlora_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from rank_adapter_linear_nf4_b300 import build, qlora
+    build.build()
+    return qlora.load_library()
+
+
+def declared_functions():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(qlora_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("qlora_quantize_nf4", "qlora_dequant_nf4", "qlora_linear_fwd",
+                     "qlora_linear_bwd", "qlora_workspace_bytes", "qlora_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_codebook_equals_oracle(lib):
+    from rank_adapter_linear_nf4_b300 import qlora
+    assert np.array_equal(np.float32(qlora.qlora_nf4_codebook()), O.NF4_CODE)
+
+
+def test_status_strings(lib):
+    from rank_adapter_linear_nf4_b300 import qlora
+    for code, name in qlora.STATUS_NAMES.items():
+        assert qlora.qlora_status_string(code).startswith(name)
+
+
+def test_workspace_bytes(lib):
+    from rank_adapter_linear_nf4_b300 import qlora
+    assert qlora.qlora_workspace_bytes(64, 256, 256, 8) > 0
+    # A pad + B^T + two [M, rp] buffers, rp = 64
+    assert qlora.qlora_workspace_bytes(4096, 4096, 4096, 16) >= (4096 + 4096 + 2 * 4096) * 64 * 2
+    assert qlora.qlora_workspace_bytes(64, 100, 256, 8) == 0      # d_in % 64
+    assert qlora.qlora_workspace_bytes(64, 256, 252, 8) == 0      # d_out % 8
+    assert qlora.qlora_workspace_bytes(64, 256, 256, 0) == 0
+    assert qlora.qlora_workspace_bytes(64, 256, 256, 129) == 0
+
+
+FAKE = 0x10000      # 16-byte aligned, never dereferenced: validation fails first
+MISALIGNED = 0x10008
+
+
+def _fwd(lib, X=FAKE, M=64, K=256, N=256, P=FAKE, S=FAKE, A=FAKE, B=FAKE, r=8, Y=FAKE, XA=FAKE,
+         ws=FAKE, ws_bytes=1 << 30):
+    return lib.qlora_linear_fwd(X, M, K, N, P, S, A, B, r, 2.0, Y, XA, ws, ws_bytes, None)
+
+
+def test_forward_argument_validation(lib):
+    assert _fwd(lib, K=100) == 4
+    assert _fwd(lib, N=260 - 2) == 4
+    assert _fwd(lib, r=0) == 4 and _fwd(lib, r=129) == 4
+    assert _fwd(lib, M=-1) == 2 and _fwd(lib, K=0) == 2
+    assert _fwd(lib, X=None) == 1 and _fwd(lib, P=None) == 1 and _fwd(lib, XA=None) == 1
+    assert _fwd(lib, X=MISALIGNED) == 3 and _fwd(lib, Y=MISALIGNED) == 3
+    assert _fwd(lib, ws=None) == 7 or _fwd(lib, ws=None) == 3
+    assert _fwd(lib, ws_bytes=16) == 7
+    assert _fwd(lib, M=0, X=None, Y=None, XA=None) == 0   # empty input launches nothing
+
+
+def test_backward_argument_validation(lib):
+    def bwd(X=FAKE, dY=FAKE, M=64, dX=FAKE, dA=FAKE, dB=FAKE, ws_bytes=1 << 30, K=256):
+        return lib.qlora_linear_bwd(X, dY, M, K, 256, FAKE, FAKE, FAKE, FAKE, 8, 2.0, FAKE,
+                                    dX, dA, dB, FAKE, ws_bytes, None)
+    assert bwd(dA=None) == 1 and bwd(dB=None) == 1 and bwd(dY=None) == 1
+    assert bwd(dX=MISALIGNED) == 3
+    assert bwd(ws_bytes=0) == 7
+    assert bwd(K=320 + 1) == 4
+
+
+def test_codec_argument_validation(lib):
+    assert lib.qlora_quantize_nf4(FAKE, 4, 100, FAKE, FAKE, None) == 4
+    assert lib.qlora_quantize_nf4(FAKE, 0, 64, FAKE, FAKE, None) == 2
+    assert lib.qlora_quantize_nf4(None, 4, 64, FAKE, FAKE, None) == 1
+    assert lib.qlora_dequant_nf4(FAKE, MISALIGNED, 4, 64, FAKE, None) == 3
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    from rank_adapter_linear_nf4_b300 import qlora
+    with pytest.raises(ValueError):
+        qlora.qlora_quantize_nf4(torch.zeros(4, 64, dtype=torch.bfloat16))
