@@ -1,0 +1,458 @@
+#!/usr/bin/env python3
+"""Benchmark: fused NF4-QLoRA linear layer, forward + backward, on B300.
+
+One step = one forward (qlora_linear_fwd) and one backward (qlora_linear_bwd)
+of the projection workload over one batch of synthetic tokens, inputs already
+resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+N > 1 is launched by torchrun: each rank runs its own independent replica of
+the workload on its own GPU (no collective on the data path; "scaling": "weak").
+`--impl reference` times the CPU oracle on the host cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused QLoRA linear fwd+bwd TFLOP/s & tokens/s; % of BF16 TC / HBM roofline"
+DEFAULT_CONFIG = "llama3_8b_q_proj"
+
+
+def shape_of(name):
+    from rank_adapter_linear_nf4_b300 import synthetic
+    return synthetic.SHAPES[name]
+
+
+def step_flops(sh) -> float:
+    """Algorithmic flops of one forward + backward (no dW: the base is frozen)."""
+    M, K, N, r = sh.M, sh.d_in, sh.d_out, sh.r
+    fwd = 2 * M * K * N + 2 * M * r * (K + N)
+    bwd = 2 * M * K * N + 4 * M * r * (K + N)
+    return float(fwd + bwd)
+
+
+def kernel_work(sh, kind):
+    """Algorithmic (flops, bytes) of one launch of a main fused kernel."""
+    M, K, N, r = sh.M, sh.d_in, sh.d_out, sh.r
+    w_bytes = 0.5625 * K * N
+    if kind == "lora_main_fwd":
+        return 2.0 * M * K * N + 2.0 * M * r * N, w_bytes + 2.0 * M * K + 2.0 * M * N + 2.0 * M * r + 2.0 * r * N
+    return 2.0 * M * K * N + 2.0 * M * r * K, w_bytes + 2.0 * M * N + 2.0 * M * K + 2.0 * M * r + 2.0 * r * K
+
+
+def workload_desc(sh) -> str:
+    kind = "rank-stabilised " if sh.rank_stabilised else ""
+    return (f"{sh.name}: M={sh.M} tokens, d_in={sh.d_in} -> d_out={sh.d_out}, r={sh.r}, "
+            f"{kind}s={sh.s:g}, NF4 blocksize 64, fwd+bwd")
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm": p["hbm_gbs"], "bf16": p["bf16_tflops"], "bf16_sust": p["bf16_tflops_sustained"],
+                "src": "measured"}
+    return {"hbm": 6400.0, "bf16": 1800.0, "bf16_sust": 1400.0, "src": "fallback"}
+
+
+# ---------------------------------------------------------------- clocks (NVML)
+
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons during the timed region:
+    NVML every ~10 ms in a thread, else `nvidia-smi -lms 100` in the background."""
+
+    REASONS = [("gpu_idle", 0x1), ("applications_clocks", 0x2), ("sw_power_cap", 0x4),
+               ("hw_slowdown", 0x8), ("sync_boost", 0x10), ("sw_thermal_slowdown", 0x20),
+               ("hw_thermal_slowdown", 0x40), ("hw_power_brake", 0x80)]
+    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active"]
+
+    def __init__(self, torch_dev: int):
+        self.mode = None
+        self.samples = []
+        self.err = ""
+        try:
+            import pynvml
+            import torch
+            pynvml.nvmlInit()
+            self.nv = pynvml
+            try:
+                uuid = str(torch.cuda.get_device_properties(torch_dev).uuid)
+                self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
+            except Exception:
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+                idx = int(vis.split(",")[torch_dev]) if vis and vis.split(",")[0].isdigit() else torch_dev
+                self.h = pynvml.nvmlDeviceGetHandleByIndex(idx)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.mode = "nvml"
+        except Exception as e:
+            self.err = f"NVML: {e!r}"
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.mode = "smi"
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+                self.smi_index = vis.split(",")[torch_dev] if vis else str(torch_dev)
+
+    def _reasons(self):
+        nv = self.nv
+        for fn in ("nvmlDeviceGetCurrentClocksEventReasons", "nvmlDeviceGetCurrentClocksThrottleReasons"):
+            if hasattr(nv, fn):
+                return int(getattr(nv, fn)(self.h))
+        return 0
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                sm = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+                pw = self.nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
+                self.samples.append((sm, pw, self._reasons()))
+            except Exception:
+                pass
+            time.sleep(0.01)
+
+    def start(self):
+        if self.mode == "nvml":
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        elif self.mode == "smi":
+            import subprocess
+            self._p = subprocess.Popen(
+                ["nvidia-smi", "-i", self.smi_index, "--query-gpu=" + ",".join(self.SMI_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+
+    def stop(self):
+        if self.mode == "nvml":
+            self._stop.set()
+            self._t.join()
+        elif self.mode == "smi":
+            self._p.terminate()
+            out, _ = self._p.communicate(timeout=10)
+            self.max_mhz = None
+            for line in out.strip().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                try:
+                    self.max_mhz = float(f[1])
+                    self.samples.append((float(f[0]), float(f[2]), int(f[3], 16)))
+                except (ValueError, IndexError):
+                    pass
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "note": "no clock source: " + self.err}
+        s = self.samples
+        mask = 0
+        for _, _, r in s:
+            mask |= r
+        reasons = [n for n, b in self.REASONS if mask & b and n != "gpu_idle"]
+        out = {"sm_mhz": statistics.median([x[0] for x in s]) if s else None,
+               "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(s),
+               "power_w_median": statistics.median([x[1] for x in s]) if s else None,
+               "source": self.mode}
+        if self.err:
+            out["note"] = self.err
+        return out
+
+
+# ---------------------------------------------------------------- oracle timing (CPU)
+
+class OracleRunner:
+    """The oracle on the first `tokens` tokens of the workload: one step is
+    NF4 dequantisation of the full weight + forward + backward (fp64)."""
+
+    def __init__(self, sh, tokens: int):
+        from oracle import qlora_oracle as O
+        from rank_adapter_linear_nf4_b300 import synthetic
+        self.O, self.sh = O, sh
+        X, dY = synthetic.activations(tokens, sh.d_in, sh.d_out, seed=0)
+        W, A, B = synthetic.weights(sh.d_in, sh.d_out, sh.r, seed=1)
+        f = lambda t: t.float().numpy()
+        self.X, self.dY, self.A, self.B = f(X), f(dY), f(A), f(B)
+        self.packed, self.absmax = O.quantize_nf4(f(W))
+        try:
+            from threadpoolctl import threadpool_info
+            self.threads = max([int(i.get("num_threads", 1)) for i in threadpool_info()] or [1])
+        except Exception:
+            self.threads = os.cpu_count() or 1
+
+    def step(self):
+        O, sh = self.O, self.sh
+        Wd = O.dequantize_nf4(self.packed, self.absmax, sh.d_out, sh.d_in)
+        _, T = O.lora_forward(self.X, Wd, self.A, self.B, sh.s)
+        O.lora_backward(self.X, self.dY, Wd, self.A, self.B, sh.s, T=T)
+
+    def time_calls(self, min_seconds: float, max_calls: int = 1000):
+        times = []
+        t_all = time.perf_counter()
+        while len(times) < max_calls:
+            t0 = time.perf_counter()
+            self.step()
+            times.append(time.perf_counter() - t0)
+            if time.perf_counter() - t_all >= min_seconds:
+                break
+        return statistics.median(times), len(times)
+
+
+def sample_shape(sh, tokens):
+    from rank_adapter_linear_nf4_b300.synthetic import LayerShape
+    return LayerShape(sh.name, tokens, sh.d_in, sh.d_out, sh.r, sh.alpha, sh.rank_stabilised)
+
+
+def cpu_baseline(sh, min_seconds=10.0):
+    tokens = min(sh.M, 256)
+    runner = OracleRunner(sh, tokens)
+    per_call, calls = runner.time_calls(min_seconds)
+    flops = step_flops(sample_shape(sh, tokens))
+    return {"value": flops / per_call / 1e12, "unit": "TFLOP/s", "cores": runner.threads, "kind": "oracle",
+            "tokens_per_s": tokens / per_call,
+            "sample": f"{tokens} of {sh.M} tokens of the same workload (NF4 dequantise of the full "
+                      f"weight + fp64 forward + backward), median of {calls} calls, "
+                      f"{per_call * 1e3:.1f} ms per call"}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    sh = shape_of(args.config)
+    tokens = min(sh.M, 128)
+    runner = OracleRunner(sh, tokens)
+    threads = runner.threads
+    for _ in range(args.warmup):
+        runner.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        runner.step()
+    elapsed = time.perf_counter() - t0
+    per_step = elapsed / max(1, args.steps)
+    sample = sample_shape(sh, tokens)
+    value = step_flops(sample) / per_step / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": per_step * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(sh), "sample_tokens_per_step": tokens},
+        "tokens_per_s": tokens / per_step,
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: {tokens} of {sh.M} tokens (dequantise + fp64 fwd + bwd)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from rank_adapter_linear_nf4_b300 import qlora, synthetic
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    sh = shape_of(args.config)
+    peaks = load_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    stream = torch.cuda.current_stream(dev)
+
+    # ---- resident input sets, rotated so that no step finds its inputs in L2
+    M, K, N, r = sh.M, sh.d_in, sh.d_out, sh.r
+    set_bytes = 2 * M * K + 2 * M * N + 0.5625 * K * N + 2 * M * K + 2 * M * N
+    n_sets = max(2, math.ceil(2.0 * l2 / set_bytes))
+    sets = []
+    ws = torch.empty(max(16, qlora.qlora_workspace_bytes(M, K, N, r)), dtype=torch.uint8, device=dev)
+    for i in range(n_sets):
+        inp = synthetic.layer_inputs(sh, seed=2 * i + 2 * rank * n_sets)
+        X, dY, W, A, B = (inp[k].to(dev) for k in ("X", "dY", "W", "A", "B"))
+        packed, absmax = qlora.qlora_quantize_nf4(W)
+        del W
+        sets.append(dict(X=X, dY=dY, packed=packed, absmax=absmax, A=A, B=B,
+                         Y=torch.empty(M, N, dtype=torch.bfloat16, device=dev),
+                         XA=torch.empty(M, r, dtype=torch.float32, device=dev),
+                         dX=torch.empty(M, K, dtype=torch.bfloat16, device=dev),
+                         dA=torch.empty(K, r, dtype=torch.float32, device=dev),
+                         dB=torch.empty(r, N, dtype=torch.float32, device=dev)))
+    torch.cuda.synchronize()
+
+    def step(i):
+        t = sets[i % n_sets]
+        qlora.qlora_linear_fwd(t["X"], t["packed"], t["absmax"], t["A"], t["B"], sh.s,
+                               Y=t["Y"], XA=t["XA"], workspace=ws)
+        qlora.qlora_linear_bwd(t["X"], t["dY"], t["packed"], t["absmax"], t["A"], t["B"], sh.s, t["XA"],
+                               dX=t["dX"], dA=t["dA"], dB=t["dB"], workspace=ws)
+
+    def timed(fn, steps):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier()
+        start.record(stream)
+        for i in range(steps):
+            fn(i)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms = start.elapsed_time(end)
+        if world > 1:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        return ms
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    # ---- official timed region
+    sampler = ClockSampler(local)
+    launches0 = qlora.qlora_launch_count()
+    sampler.start()
+    total_ms = timed(step, args.steps)
+    clocks = sampler.stop()
+    launches = qlora.qlora_launch_count() - launches0
+    if qlora.qlora_device_status(clear=True) != 0:
+        raise RuntimeError("device status word reports an error during the timed region")
+
+    ms_step = total_ms / args.steps
+    flops = step_flops(sh)
+    tflops_rank = flops / (ms_step * 1e-3) / 1e12
+    value = tflops_rank * world
+    tokens_per_s = M * world / (ms_step * 1e-3)
+
+    # ---- same region again with every library launch bracketed by CUDA events
+    qlora.qlora_profile_enable(True)
+    qlora.qlora_profile_collect()
+    prof_total_ms = timed(step, args.steps)
+    kernels = qlora.qlora_profile_collect()
+    qlora.qlora_profile_enable(False)
+    dom = max(kernels.items(), key=lambda kv: kv[1][0])[0]
+    main_kinds = [k for k in ("lora_main_fwd", "lora_main_dX") if k in kernels]
+    roof_kind = dom if dom in ("lora_main_fwd", "lora_main_dX") else (main_kinds[0] if main_kinds else dom)
+    k_ms, k_n = kernels[roof_kind]
+    k_avg_s = k_ms / k_n * 1e-3
+    kf, kb = kernel_work(sh, roof_kind)
+    ridge = peaks["bf16_sust"] * 1e12 / (peaks["hbm"] * 1e9)
+    if kf / kb >= ridge:
+        achieved = kf / k_avg_s / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sust"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_sust"], "traffic": None,
+                    "kernel": roof_kind, "peak_kind": f"bf16 dense sustained ({peaks['src']})",
+                    "frac_of_burst_peak": achieved / peaks["bf16"]}
+    else:
+        achieved = kb / k_avg_s / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm"], "traffic": None, "kernel": roof_kind,
+                    "peak_kind": f"HBM copy ({peaks['src']})"}
+    roofline["flops_per_launch"] = kf
+    roofline["algorithmic_bytes_per_launch"] = kb
+    roofline["avg_launch_us"] = k_avg_s * 1e6
+    per_kernel = {k: {"launches": n, "total_ms": round(t, 4), "avg_us": round(t / n * 1e3, 2),
+                      "share": round(t / sum(v[0] for v in kernels.values()), 4)}
+                  for k, (t, n) in sorted(kernels.items(), key=lambda kv: -kv[1][0])}
+
+    # ---- end to end: pinned host buffers, copies inside the timed region
+    t0 = sets[0]
+    hX = t0["X"].cpu().pin_memory()
+    hdY = t0["dY"].cpu().pin_memory()
+    hY = torch.empty_like(t0["Y"], device="cpu").pin_memory()
+    hdX = torch.empty_like(t0["dX"], device="cpu").pin_memory()
+    hdA = torch.empty_like(t0["dA"], device="cpu").pin_memory()
+    hdB = torch.empty_like(t0["dB"], device="cpu").pin_memory()
+    dX_in, dY_in = torch.empty_like(t0["X"]), torch.empty_like(t0["dY"])
+
+    def e2e_step(i):
+        dX_in.copy_(hX, non_blocking=True)
+        dY_in.copy_(hdY, non_blocking=True)
+        qlora.qlora_linear_fwd(dX_in, t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
+                               Y=t0["Y"], XA=t0["XA"], workspace=ws)
+        qlora.qlora_linear_bwd(dX_in, dY_in, t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
+                               t0["XA"], dX=t0["dX"], dA=t0["dA"], dB=t0["dB"], workspace=ws)
+        hY.copy_(t0["Y"], non_blocking=True)
+        hdX.copy_(t0["dX"], non_blocking=True)
+        hdA.copy_(t0["dA"], non_blocking=True)
+        hdB.copy_(t0["dB"], non_blocking=True)
+
+    e2e_step(0)
+    e2e_steps = max(3, min(args.steps, 200))
+    e2e_ms = timed(e2e_step, e2e_steps) / e2e_steps
+    h2d = hX.numel() * 2 + hdY.numel() * 2
+    d2h = hY.numel() * 2 + hdX.numel() * 2 + hdA.numel() * 4 + hdB.numel() * 4
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(sh),
+                   "l2": f"inputs rotated over {n_sets} resident sets of {set_bytes / 1e6:.0f} MB "
+                         f"(> 2x the {l2 / 1e6:.0f} MB L2)",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": tokens_per_s,
+        "frac_of_bf16_peak_whole_step": {"sustained": tflops_rank / peaks["bf16_sust"],
+                                         "burst": tflops_rank / peaks["bf16"]},
+        "roofline": roofline,
+        "kernels": per_kernel,
+        "profiled_ms_per_step": prof_total_ms / args.steps,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(sh, min_seconds=args.cpu_seconds)
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -81,6 +81,19 @@ void qlora_nf4_codebook(float out[16]);
  * synchronisation or the read fails. */
 qlora_status qlora_device_status(int* code, int clear);
 
+/* Launch accounting for measurement tools.
+ * qlora_profile_enable(1): from now on every kernel the library launches is
+ * bracketed by two CUDA events recorded on the launching stream (events are
+ * created on first use and reused; no device memory is allocated).
+ * qlora_profile_collect: waits for the recorded events, writes for each kernel
+ * kind launched since the last collect its name (static string), total
+ * device milliseconds and launch count, returns the number of kinds written
+ * (at most max_kinds), and clears the records.  Returns -1 on a CUDA error.
+ * qlora_launch_count: kernels launched by this library since it was loaded. */
+qlora_status qlora_profile_enable(int enable);
+int qlora_profile_collect(const char** names, float* total_ms, int* launches, int max_kinds);
+int64_t qlora_launch_count(void);
+
 /*
  * NF4 quantisation of a bf16 weight (offline; once per weight).
  *   W       [n_out, n_in] bf16, read.

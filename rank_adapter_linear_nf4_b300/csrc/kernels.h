@@ -8,6 +8,29 @@
 
 namespace qlora {
 
+// Kernel kinds for launch accounting (names in qlora_api.cu).
+enum KernelKind : int {
+  kKindQuantize = 0,
+  kKindDequant,
+  kKindPrep,
+  kKindRowsT,
+  kKindRowsG,
+  kKindRed,
+  kKindMainFwd,
+  kKindMainDx,
+  kNumKernelKinds
+};
+
+// Brackets one kernel launch: counts it and, when profiling is enabled,
+// records CUDA events around it on `stream`.
+struct LaunchScope {
+  LaunchScope(int kind, cudaStream_t stream);
+  ~LaunchScope();
+  int kind;
+  cudaStream_t stream;
+  int slot;
+};
+
 // NF4 codec (nf4_codec.cu).
 cudaError_t launch_quantize_nf4(const uint16_t* W, int64_t n_elems, uint8_t* packed, float* absmax,
                                 cudaStream_t stream);
@@ -27,8 +50,7 @@ struct LayerDims {
 
 // Workspace carve-up shared by the forward and the backward.
 struct Workspace {
-  uint16_t* a_pad;   // [K, rp]  A with zero columns r..rp-1
-  uint16_t* b_t;     // [N, rp]  B transposed, zero columns r..rp-1
+  uint16_t* a_pad;   // [K, rp]  A with zero columns r..rp-1 (used when r % 8 != 0)
   uint16_t* s_t;     // [M, rp]  bf16(s * X.A), zero-padded
   uint16_t* s_g;     // [M, rp]  bf16(s * dY.B^T), zero-padded
 };

@@ -123,6 +123,7 @@ cudaError_t launch_quantize_nf4(const uint16_t* W, int64_t n_elems, uint8_t* pac
   static const Thresholds th = make_thresholds();
   const int64_t n_groups = n_elems / 8;
   const int64_t grid = (n_groups + 255) / 256;
+  LaunchScope scope(kKindQuantize, stream);
   nf4_quantize_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(
       reinterpret_cast<const uint4*>(W), n_groups, reinterpret_cast<uint32_t*>(packed), absmax, th);
   return cudaGetLastError();
@@ -132,6 +133,7 @@ cudaError_t launch_dequant_nf4(const uint8_t* packed, const float* absmax, int64
                                uint16_t* W_out, cudaStream_t stream) {
   const int64_t n_blocks = n_elems / 64;
   const int64_t grid = (n_blocks + kDeqThreads - 1) / kDeqThreads;
+  LaunchScope scope(kKindDequant, stream);
   nf4_dequant_kernel<<<static_cast<unsigned>(grid), kDeqThreads, 0, stream>>>(
       reinterpret_cast<const uint4*>(packed), absmax, n_blocks, reinterpret_cast<uint4*>(W_out));
   return cudaGetLastError();

@@ -1,6 +1,9 @@
 // qlora_api.cu -- the C ABI (include/qlora.h): argument validation, status
 // codes, the device status word, and launch sequencing on the caller's stream.
+#include <atomic>
 #include <cstdint>
+#include <mutex>
+#include <vector>
 #include <cuda_runtime.h>
 
 #include "../../include/qlora.h"
@@ -67,9 +70,95 @@ qlora::LayerDims dims_of(int64_t M, int64_t d_in, int64_t d_out, int32_t r, floa
   return d;
 }
 
+// ---------------------------------------------------------------- launch accounting
+
+std::atomic<int64_t> g_launches{0};
+std::atomic<bool> g_profiling{false};
+
+struct ProfRecord {
+  int kind;
+  cudaEvent_t begin, end;
+};
+
+std::mutex g_prof_mu;
+std::vector<ProfRecord> g_records;     // recorded since the last collect
+std::vector<cudaEvent_t> g_free_events;
+
+const char* const kKindNames[qlora::kNumKernelKinds] = {
+    "nf4_quantize", "nf4_dequant", "lora_pad_A", "lora_rows_T", "lora_rows_G",
+    "lora_red_dA_dB", "lora_main_fwd", "lora_main_dX"};
+
+cudaEvent_t take_event() {
+  if (!g_free_events.empty()) {
+    cudaEvent_t e = g_free_events.back();
+    g_free_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
 }  // namespace
 
+namespace qlora {
+
+LaunchScope::LaunchScope(int k, cudaStream_t s) : kind(k), stream(s), slot(-1) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (!g_profiling.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  ProfRecord r{k, take_event(), take_event()};
+  if (r.begin == nullptr || r.end == nullptr) return;
+  if (cudaEventRecord(r.begin, s) != cudaSuccess) return;
+  slot = static_cast<int>(g_records.size());
+  g_records.push_back(r);
+}
+
+LaunchScope::~LaunchScope() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  cudaEventRecord(g_records[slot].end, stream);
+}
+
+}  // namespace qlora
+
 extern "C" {
+
+qlora_status qlora_profile_enable(int enable) {
+  g_profiling.store(enable != 0);
+  return QLORA_OK;
+}
+
+int qlora_profile_collect(const char** names, float* total_ms, int* launches, int max_kinds) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  float ms[qlora::kNumKernelKinds] = {0};
+  int cnt[qlora::kNumKernelKinds] = {0};
+  bool failed = false;
+  for (const ProfRecord& r : g_records) {
+    float t = 0.0f;
+    if (cudaEventSynchronize(r.end) != cudaSuccess ||
+        cudaEventElapsedTime(&t, r.begin, r.end) != cudaSuccess)
+      failed = true;
+    ms[r.kind] += t;
+    cnt[r.kind] += 1;
+    g_free_events.push_back(r.begin);
+    g_free_events.push_back(r.end);
+  }
+  g_records.clear();
+  if (failed) return -1;
+  int n = 0;
+  for (int k = 0; k < qlora::kNumKernelKinds && n < max_kinds; ++k) {
+    if (cnt[k] == 0) continue;
+    if (names) names[n] = kKindNames[k];
+    if (total_ms) total_ms[n] = ms[k];
+    if (launches) launches[n] = cnt[k];
+    ++n;
+  }
+  return n;
+}
+
+int64_t qlora_launch_count(void) { return g_launches.load(); }
+
 
 const char* qlora_status_string(qlora_status status) {
   switch (status) {

@@ -29,6 +29,10 @@ _SIGNATURES = {
     "qlora_last_cuda_error": (ctypes.c_int, []),
     "qlora_nf4_codebook": (None, [ctypes.POINTER(ctypes.c_float)]),
     "qlora_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
+    "qlora_profile_enable": (ctypes.c_int, [ctypes.c_int]),
+    "qlora_profile_collect": (ctypes.c_int, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float),
+                                             ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
+    "qlora_launch_count": (ctypes.c_int64, []),
     "qlora_quantize_nf4": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
     "qlora_dequant_nf4": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
     "qlora_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32]),
@@ -103,6 +107,27 @@ def qlora_device_status(clear: bool = True) -> int:
     code = ctypes.c_int(0)
     _check("qlora_device_status", load_library().qlora_device_status(ctypes.byref(code), int(clear)))
     return code.value
+
+
+def qlora_profile_enable(enable: bool = True) -> None:
+    """Bracket every library kernel launch with CUDA events (launch accounting)."""
+    _check("qlora_profile_enable", load_library().qlora_profile_enable(int(enable)))
+
+
+def qlora_profile_collect() -> dict:
+    """Per kernel kind since the last collect: {name: (total_ms, launches)}."""
+    n_max = 16
+    names = (ctypes.c_char_p * n_max)()
+    ms = (ctypes.c_float * n_max)()
+    cnt = (ctypes.c_int * n_max)()
+    n = load_library().qlora_profile_collect(names, ms, cnt, n_max)
+    if n < 0:
+        raise QloraError("qlora_profile_collect", 5)
+    return {names[i].decode(): (float(ms[i]), int(cnt[i])) for i in range(n)}
+
+
+def qlora_launch_count() -> int:
+    return int(load_library().qlora_launch_count())
 
 
 def qlora_workspace_bytes(M: int, d_in: int, d_out: int, r: int) -> int:

@@ -56,8 +56,8 @@ def test_status_strings(lib):
 def test_workspace_bytes(lib):
     from rank_adapter_linear_nf4_b300 import qlora
     assert qlora.qlora_workspace_bytes(64, 256, 256, 8) > 0
-    # A pad + B^T + two [M, rp] buffers, rp = 64
-    assert qlora.qlora_workspace_bytes(4096, 4096, 4096, 16) >= (4096 + 4096 + 2 * 4096) * 64 * 2
+    # padded A + two [M, rp] bf16 buffers, rp = 64
+    assert qlora.qlora_workspace_bytes(4096, 4096, 4096, 16) >= (4096 + 2 * 4096) * 64 * 2
     assert qlora.qlora_workspace_bytes(64, 100, 256, 8) == 0      # d_in % 64
     assert qlora.qlora_workspace_bytes(64, 256, 252, 8) == 0      # d_out % 8
     assert qlora.qlora_workspace_bytes(64, 256, 256, 0) == 0
