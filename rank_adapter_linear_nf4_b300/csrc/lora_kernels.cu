@@ -71,15 +71,15 @@ __global__ void __launch_bounds__(256) lora_prep_kernel(const PrepParams p) {
 // kRed:   job 0  dA = X^T . bf16(s*G)    job 1  dB = (bf16(s*T))^T . dY   (both operands MN-major)
 enum SkinnyMode : int { kRowsT = 0, kRowsG = 1, kRed = 2 };
 
-constexpr int kSkStages = 6;
 constexpr int kSkThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 
 template <int RP>
 struct SkinnySmem {
+  static constexpr int kStages = RP == 64 ? 8 : 6;   // as many stages as fit: keeps HBM reads in flight
   static constexpr int kABytes = kTileP * 128;   // 128 rows x 64 bf16
   static constexpr int kBBytes = RP * 128;       // RP columns x 64 bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kBarOffset = kSkStages * kStageBytes;
+  static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kBytes = kBarOffset + 256 + 1024;
   static constexpr int kRedStride = RP + 4;      // floats per reduction row: 16-B rows, spread banks
   static_assert(kTileP * kRedStride * 4 <= kBarOffset, "reduction buffer must fit");
@@ -123,7 +123,7 @@ __device__ __forceinline__ uint2 bf16x4_scaled(float s, float4 v) {
   return o;
 }
 
-template <int MODE, int RP>
+template <int MODE, int RP, int NSPLIT>
 __global__ void __launch_bounds__(kSkThreads, 1)
     lora_skinny_kernel(const __grid_constant__ CUtensorMap map_a0,
                        const __grid_constant__ CUtensorMap map_b0,
@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   const uint32_t bar0 = base + S::kBarOffset;
-  const uint32_t accum_bar = bar0 + 8u * (2 * kSkStages);
+  const uint32_t accum_bar = bar0 + 8u * (2 * S::kStages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int job = (MODE == kRed && static_cast<int>(blockIdx.x) >= p.job[0].tiles) ? 1 : 0;
@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const CUtensorMap* map_a = job ? &map_a1 : &map_a0;
   const CUtensorMap* map_b = job ? &map_b1 : &map_b0;
   const int p0 = (static_cast<int>(blockIdx.x) - (job ? p.job[0].tiles : 0)) * kTileP;
-  const uint32_t nsplit = gridDim.y;
+  constexpr uint32_t nsplit = NSPLIT;   // == gridDim.y == cluster size
   const uint32_t split = blockIdx.y;
   const int ct_begin = static_cast<int>((static_cast<int64_t>(p.num_ct) * split) / nsplit);
   const int ct_end = static_cast<int>((static_cast<int64_t>(p.num_ct) * (split + 1)) / nsplit);
@@ -160,9 +160,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int i = 0; i < kSkStages; ++i) {
+    for (int i = 0; i < S::kStages; ++i) {
       mbar_init(bar0 + 8u * i, 1);                    // full
-      mbar_init(bar0 + 8u * (kSkStages + i), 1);      // empty
+      mbar_init(bar0 + 8u * (S::kStages + i), 1);      // empty
     }
     mbar_init(accum_bar, 1);
     fence_barrier_init();
@@ -181,9 +181,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     if (lane == 0) {
       int i = 0;
       for (; i < nct; ++i) {
-        const int slot = i % kSkStages;
-        const uint32_t ph = (i / kSkStages) & 1;
-        if (!mbar_wait(bar0 + 8u * (kSkStages + slot), ph ^ 1, ab)) break;
+        const int slot = i % S::kStages;
+        const uint32_t ph = (i / S::kStages) & 1;
+        if (!mbar_wait(bar0 + 8u * (S::kStages + slot), ph ^ 1, ab)) break;
         const int ct = ct_begin + i;
         const uint32_t a = base + slot * S::kStageBytes;
         const uint32_t b = a + S::kABytes;
@@ -202,16 +202,16 @@ __global__ void __launch_bounds__(kSkThreads, 1)
           tma_load_2d(b, map_b, full, ct * kTileK, 0);
         }
       }
-      for (int q = i - 1; q >= 0 && q >= i - kSkStages; --q)
-        mbar_wait(bar0 + 8u * (q % kSkStages), (q / kSkStages) & 1, ab, false);
+      for (int q = i - 1; q >= 0 && q >= i - S::kStages; --q)
+        mbar_wait(bar0 + 8u * (q % S::kStages), (q / S::kStages) & 1, ab, false);
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(kTileP, RP, kAmn ? 1 : 0, kBmn ? 1 : 0);
       for (int i = 0; i < nct; ++i) {
-        const int slot = i % kSkStages;
-        const uint32_t ph = (i / kSkStages) & 1;
+        const int slot = i % S::kStages;
+        const uint32_t ph = (i / S::kStages) & 1;
         if (!mbar_wait(bar0 + 8u * slot, ph, ab)) break;
         tc_fence_after_sync();
         const uint32_t a = base + slot * S::kStageBytes;
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
           const uint64_t bd = kBmn ? sw128_desc(b + kk * 2048, 8192, 1024) : sw128_desc(b + kk * 32, 16, 1024);
           umma_bf16(tmem_d, ad, bd, idesc, (i | kk) != 0 ? 1u : 0u);
         }
-        umma_commit(bar0 + 8u * (kSkStages + slot));
+        umma_commit(bar0 + 8u * (S::kStages + slot));
       }
       umma_commit(accum_bar);
     }
@@ -255,69 +255,92 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   cluster_sync_all();
 
   if (warp >= 2 && s_abort == 0) {
+    // Sum the NSPLIT partial tiles in rank order.  Every remote load of a pass is
+    // issued before any is consumed, so the pass costs one DSMEM round trip.
     const int t = threadIdx.x - 64;   // 0..127
     const uint32_t rank = cluster_ctarank();
-    const int rows_per = kTileP / static_cast<int>(nsplit);
-    const int row_begin = static_cast<int>(rank) * rows_per;
-    constexpr int kGroups = RP / 4;
+    constexpr int kRowsPer = kTileP / NSPLIT;
+    constexpr int kGroups = RP / 4;                      // float4 column groups per row
+    constexpr int kItemsPerPass = 16 / NSPLIT;           // (row, group) items per thread per pass
+    constexpr int kPasses = (kRowsPer * kGroups) / (128 * kItemsPerPass);
+    const int row_begin = static_cast<int>(rank) * kRowsPer;
     const bool transposed = (MODE == kRed && job == 1);
-    for (int e = t; e < rows_per * kGroups; e += 128) {
-      int lr, cg;
-      if (transposed) {   // dB [r, rows]: consecutive threads take consecutive rows
-        cg = e / rows_per;
-        lr = e % rows_per;
-      } else {
-        lr = e / kGroups;
-        cg = e % kGroups;
-      }
-      const int row = row_begin + lr;
-      const int grow = p0 + row;
-      if (grow >= j_rows) continue;
-      const int col = cg * 4;
-      const uint32_t local = base + static_cast<uint32_t>(row * S::kRedStride + col) * 4u;
-      float4 part[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (q < static_cast<int>(nsplit)) part[q] = ld_dsmem_v4(map_to_cta(local, q));
-      float4 sum = part[0];
+    for (int pass = 0; pass < kPasses; ++pass) {
+      float4 part[kItemsPerPass][NSPLIT];
+      int rows[kItemsPerPass], cols[kItemsPerPass];
 #pragma unroll
-      for (int q = 1; q < 8; ++q)
-        if (q < static_cast<int>(nsplit)) {
-          sum.x += part[q].x;
-          sum.y += part[q].y;
-          sum.z += part[q].z;
-          sum.w += part[q].w;
+      for (int it = 0; it < kItemsPerPass; ++it) {
+        const int e = t + (pass * kItemsPerPass + it) * 128;
+        int lr, cg;
+        if (transposed) {   // dB [r, rows]: consecutive threads take consecutive rows
+          cg = e / kRowsPer;
+          lr = e % kRowsPer;
+        } else {
+          lr = e / kGroups;
+          cg = e % kGroups;
         }
-      const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
-      if (MODE == kRowsT) {
+        rows[it] = row_begin + lr;
+        cols[it] = cg * 4;
+        const uint32_t local = base + static_cast<uint32_t>(rows[it] * S::kRedStride + cols[it]) * 4u;
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (col + c < p.r) j_out_f32[static_cast<int64_t>(grow) * p.r + col + c] = vals[c];
-        *reinterpret_cast<uint2*>(j_out_bf16 + static_cast<int64_t>(grow) * RP + col) = bf16x4_scaled(p.s, sum);
-      } else if (MODE == kRowsG) {
-        *reinterpret_cast<uint2*>(j_out_bf16 + static_cast<int64_t>(grow) * RP + col) = bf16x4_scaled(p.s, sum);
-      } else if (!transposed) {
+        for (int q = 0; q < NSPLIT; ++q) part[it][q] = ld_dsmem_v4(map_to_cta(local, q));
+      }
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (col + c < p.r) j_out_f32[static_cast<int64_t>(grow) * p.r + col + c] = vals[c];
-      } else {
+      for (int it = 0; it < kItemsPerPass; ++it) {
+        const int grow = p0 + rows[it];
+        if (grow >= j_rows) continue;
+        const int col = cols[it];
+        float4 sum = part[it][0];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          if (col + c < p.r) j_out_f32[static_cast<int64_t>(col + c) * j_rows + grow] = vals[c];
+        for (int q = 1; q < NSPLIT; ++q) {
+          sum.x += part[it][q].x;
+          sum.y += part[it][q].y;
+          sum.z += part[it][q].z;
+          sum.w += part[it][q].w;
+        }
+        const float vals[4] = {sum.x, sum.y, sum.z, sum.w};
+        if (MODE == kRowsT) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (col + c < p.r) j_out_f32[static_cast<int64_t>(grow) * p.r + col + c] = vals[c];
+          *reinterpret_cast<uint2*>(j_out_bf16 + static_cast<int64_t>(grow) * RP + col) = bf16x4_scaled(p.s, sum);
+        } else if (MODE == kRowsG) {
+          *reinterpret_cast<uint2*>(j_out_bf16 + static_cast<int64_t>(grow) * RP + col) = bf16x4_scaled(p.s, sum);
+        } else if (!transposed) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (col + c < p.r) j_out_f32[static_cast<int64_t>(grow) * p.r + col + c] = vals[c];
+        } else {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (col + c < p.r) j_out_f32[static_cast<int64_t>(col + c) * j_rows + grow] = vals[c];
+        }
       }
     }
     if (MODE == kRowsG) {
-      // bf16(s*T) for the same rows, from the fp32 T saved by the forward
-      for (int e = t; e < rows_per * kGroups; e += 128) {
-        const int grow = p0 + row_begin + e / kGroups;
-        if (grow >= j_rows) continue;
-        const int col = (e % kGroups) * 4;
-        float v[4];
+      // bf16(s*T) for the same rows, from the fp32 T saved by the forward (loads first, then stores)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          v[c] = (col + c < p.r) ? p.xa[static_cast<int64_t>(grow) * p.r + col + c] : 0.0f;
-        *reinterpret_cast<uint2*>(p.s_t + static_cast<int64_t>(grow) * RP + col) =
-            bf16x4_scaled(p.s, make_float4(v[0], v[1], v[2], v[3]));
+      for (int pass = 0; pass < kPasses; ++pass) {
+        float v[kItemsPerPass][4];
+#pragma unroll
+        for (int it = 0; it < kItemsPerPass; ++it) {
+          const int e = t + (pass * kItemsPerPass + it) * 128;
+          const int grow = p0 + row_begin + e / kGroups;
+          const int col = (e % kGroups) * 4;
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            v[it][c] = (grow < j_rows && col + c < p.r) ? __ldg(p.xa + static_cast<int64_t>(grow) * p.r + col + c) : 0.0f;
+        }
+#pragma unroll
+        for (int it = 0; it < kItemsPerPass; ++it) {
+          const int e = t + (pass * kItemsPerPass + it) * 128;
+          const int grow = p0 + row_begin + e / kGroups;
+          if (grow >= j_rows) continue;
+          const int col = (e % kGroups) * 4;
+          *reinterpret_cast<uint2*>(p.s_t + static_cast<int64_t>(grow) * RP + col) =
+              bf16x4_scaled(p.s, make_float4(v[it][0], v[it][1], v[it][2], v[it][3]));
+        }
       }
     }
   }
@@ -335,35 +358,54 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
 // ============================================================== main fused GEMM
 
-constexpr int kMainStages = 4;
-constexpr int kMainThreads = 320;   // warp 0 TMA, warp 1 MMA, warps 2-9 dequant + epilogue
+constexpr int kMainStages = 4;       // X / W operand stages
+constexpr int kRawStages = 4;        // NF4 code + absmax stages (TMA); same count, so stage g uses slot g % 4 in both
+constexpr int kEpiChunk = 32;        // tokens per epilogue store
+// warp 0: TMA for the token operand; warp 1: MMA; warps 2-9: dequant; warps 10-13: epilogue;
+// warp 14: TMA for the NF4 codes and absmax (its own ring, so code latency never holds up operand loads)
+constexpr int kMainThreads = 480;
 
 template <int BN>
 struct MainSmem {
   static constexpr int kActBytes = BN * 128;      // BN tokens x 64 contraction
   static constexpr int kWBytes = kTileP * 128;    // 128 features x 64 contraction
   static constexpr int kStageBytes = kActBytes + kWBytes;
-  static constexpr int kBarOffset = kMainStages * kStageBytes;
+  static constexpr int kCodeBytes = 4096;         // Y: 128 rows x 32 B; dX: 64 rows x 64 B
+  static constexpr int kAbsBytes = 2048;          // Y: 128 rows x 4 fp32; dX: 64 rows x 4 fp32
+  static constexpr int kRawBytes = kCodeBytes + kAbsBytes;
+  static constexpr int kRawOffset = kMainStages * kStageBytes;
+  static constexpr int kChunkBytes = kEpiChunk * kTileP * 2;   // two [32 tokens][64 features] halves
+  static constexpr int kStagingOffset = kRawOffset + kRawStages * kRawBytes;
+  static constexpr int kBarOffset = kStagingOffset + kChunkBytes;
   static constexpr int kBytes = kBarOffset + 256 + 1024;
-  static_assert(BN * kTileP * 2 <= kBarOffset, "epilogue staging must fit");
+  static_assert(kBytes <= 232448, "shared memory budget");
 };
 
 struct MainParams {
-  const uint8_t* packed;   // NF4 codes of W [N, K]
-  const float* absmax;     // [N * K / 64]
+  const float* absmax;     // [N * K / 64], read directly when kAbsTma is false
+  int M;                   // tokens
   int K;                   // d_in
   int N;                   // d_out
-  int num_kt;              // NF4 stages
-  int num_lt;              // LoRA stages
+  int num_kt;              // NF4 stages per tile
+  int num_lt;              // LoRA stages per tile
+  int p_tiles;             // output-feature tiles of 128
+  int t_tiles;             // token tiles of BN
   int* status;
 };
 
-template <int BN, bool kTrans>
+// Persistent: CTA c takes tiles c, c + gridDim.x, ...; tile id = token_tile * p_tiles + feature_tile.
+// Two TMEM accumulators let the epilogue of one tile overlap the main loop of the next.
+// NF4 codes (and, when kAbsTma, the absmax values) of each stage arrive by TMA in a
+// ring of their own; TMA zero-fills rows and columns outside W, so outside W the
+// dequantised operand is zero without per-thread bounds checks.
+template <int BN, bool kTrans, bool kAbsTma>
 __global__ void __launch_bounds__(kMainThreads, 1)
     lora_main_kernel(const __grid_constant__ CUtensorMap map_act,    // X or dY, box {64, BN}
                      const __grid_constant__ CUtensorMap map_lact,   // bf16(s*T) or bf16(s*G), box {64, BN}
                      const __grid_constant__ CUtensorMap map_lw,     // Y: B [r, N], box {64, 64}; dX: A [K, r], box {64, 128}
-                     const __grid_constant__ CUtensorMap map_out,    // Y or dX, box {128, BN}
+                     const __grid_constant__ CUtensorMap map_out,    // Y or dX, box {64, 32}, 128-B swizzle
+                     const __grid_constant__ CUtensorMap map_code,   // packed [N, K/2] bytes; Y box {32, 128}, dX box {64, 64}
+                     const __grid_constant__ CUtensorMap map_abs,    // absmax [N, K/64]; Y box {4, 128}, dX box {4, 64}
                      const MainParams p) {
   using S = MainSmem<BN>;
   extern __shared__ uint8_t smem_raw[];
@@ -373,23 +415,40 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   const uint32_t bar0 = base + S::kBarOffset;
-  // barriers: full_act[st], full_w[st], empty[st], accum
-  const uint32_t accum_bar = bar0 + 8u * (3 * kMainStages);
+  auto full_act = [&](int i) { return bar0 + 8u * i; };
+  auto full_w = [&](int i) { return bar0 + 8u * (kMainStages + i); };
+  auto empty = [&](int i) { return bar0 + 8u * (2 * kMainStages + i); };
+  auto raw_full = [&](int i) { return bar0 + 8u * (3 * kMainStages + i); };
+  auto raw_empty = [&](int i) { return bar0 + 8u * (3 * kMainStages + kRawStages + i); };
+  auto tmem_full = [&](int a) { return bar0 + 8u * (3 * kMainStages + 2 * kRawStages + a); };
+  auto tmem_empty = [&](int a) { return bar0 + 8u * (3 * kMainStages + 2 * kRawStages + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (3 * kMainStages + 2 * kRawStages + 4);
+  auto raw_slot = [&](int i) { return base + S::kRawOffset + static_cast<uint32_t>(i * S::kRawBytes); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int p0 = blockIdx.x * kTileP;
-  const int t0 = blockIdx.y * BN;
   const int total = p.num_kt + p.num_lt;
+  const int num_tiles = p.p_tiles * p.t_tiles;
+  const int grid = static_cast<int>(gridDim.x);
+  const int tiles_here = (num_tiles - static_cast<int>(blockIdx.x) + grid - 1) / grid;
+  const int g_end = tiles_here * total;   // stages this CTA runs
   Abort ab{&s_abort, p.status};
 
   if (threadIdx.x == 0) {
     s_abort = 0;
     for (int i = 0; i < kMainStages; ++i) {
-      mbar_init(bar0 + 8u * i, 1);                          // full_act: TMA bytes
-      mbar_init(bar0 + 8u * (kMainStages + i), 4);          // full_w: the 4 warps of one dequant group
-      mbar_init(bar0 + 8u * (2 * kMainStages + i), 1);      // empty: MMA commit
+      mbar_init(full_act(i), 1);    // TMA transaction bytes
+      mbar_init(full_w(i), 4);      // the 4 warps of one dequant group
+      mbar_init(empty(i), 1);       // MMA commit
     }
-    mbar_init(accum_bar, 1);
+    for (int i = 0; i < kRawStages; ++i) {
+      mbar_init(raw_full(i), 1);    // TMA transaction bytes (or a plain arrive for LoRA stages)
+      mbar_init(raw_empty(i), 4);   // the 4 warps of the group that reads the slot
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tmem_full(a), 1);   // MMA commit
+      mbar_init(tmem_empty(a), 4);  // the 4 epilogue warps
+    }
+    mbar_init(drain_bar, 1);
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -397,42 +456,85 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     tma_prefetch_map(&map_lact);
     tma_prefetch_map(&map_lw);
     tma_prefetch_map(&map_out);
+    tma_prefetch_map(&map_code);
+    if (kAbsTma) tma_prefetch_map(&map_abs);
   }
-  if (warp == 1) tmem_alloc(smem_u32(&s_tmem), BN);
+  if (warp == 1) tmem_alloc(smem_u32(&s_tmem), 2 * BN);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem_d = s_tmem;
+  const uint32_t tmem_base = s_tmem;
 
   if (warp == 0) {
-    // ---------------- TMA producer
+    // ---------------- TMA producer for the token operand (and the LoRA stages)
     if (lane == 0) {
-      int s = 0;
-      for (; s < total; ++s) {
-        const int slot = s % kMainStages;
-        const uint32_t ph = (s / kMainStages) & 1;
-        if (!mbar_wait(bar0 + 8u * (2 * kMainStages + slot), ph ^ 1, ab)) break;
+      int g = 0;
+      int s = 0, p0 = static_cast<int>(blockIdx.x % p.p_tiles) * kTileP;
+      int t0 = static_cast<int>(blockIdx.x / p.p_tiles) * BN;
+      int tile = blockIdx.x;
+      for (; g < g_end; ++g) {
+        const int slot = g & (kMainStages - 1);
+        if (!mbar_wait(empty(slot), ((g / kMainStages) & 1) ^ 1, ab)) break;
         const uint32_t act = base + slot * S::kStageBytes;
-        const uint32_t full = bar0 + 8u * slot;
         if (s < p.num_kt) {
-          mbar_arrive_expect_tx(full, S::kActBytes);
-          tma_load_2d(act, &map_act, full, s * kTileK, t0);
+          mbar_arrive_expect_tx(full_act(slot), S::kActBytes);
+          tma_load_2d(act, &map_act, full_act(slot), s * kTileK, t0);
         } else {
           const int j = s - p.num_kt;
-          mbar_arrive_expect_tx(full, S::kActBytes + S::kWBytes);
-          tma_load_2d(act, &map_lact, full, j * kTileK, t0);
+          mbar_arrive_expect_tx(full_act(slot), S::kActBytes + S::kWBytes);
+          tma_load_2d(act, &map_lact, full_act(slot), j * kTileK, t0);
           if (kTrans) {
             // A [K, r] rows p0..p0+127, LoRA columns 64j..: K-major
-            tma_load_2d(act + S::kActBytes, &map_lw, full, j * kTileK, p0);
+            tma_load_2d(act + S::kActBytes, &map_lw, full_act(slot), j * kTileK, p0);
           } else {
             // B [r, N] rows 64j.. (the LoRA contraction), columns p0..p0+127: MN-major
-            tma_load_2d(act + S::kActBytes, &map_lw, full, p0, j * kTileK);
-            tma_load_2d(act + S::kActBytes + 8192, &map_lw, full, p0 + 64, j * kTileK);
+            tma_load_2d(act + S::kActBytes, &map_lw, full_act(slot), p0, j * kTileK);
+            tma_load_2d(act + S::kActBytes + 8192, &map_lw, full_act(slot), p0 + 64, j * kTileK);
           }
         }
+        if (++s == total) {
+          s = 0;
+          tile += grid;
+          p0 = (tile % p.p_tiles) * kTileP;
+          t0 = (tile / p.p_tiles) * BN;
+        }
       }
-      for (int q = s - 1; q >= 0 && q >= s - kMainStages; --q)
-        mbar_wait(bar0 + 8u * (q % kMainStages), (q / kMainStages) & 1, ab, false);
+      // wait (bounded) until every issued load has landed
+      for (int q = g - 1; q >= 0 && q >= g - kMainStages; --q)
+        mbar_wait(full_act(q % kMainStages), (q / kMainStages) & 1, ab, false);
+    }
+    __syncwarp();
+  } else if (warp == 14) {
+    // ---------------- TMA producer for the NF4 codes and absmax
+    if (lane == 0) {
+      int g = 0;
+      int s = 0, p0 = static_cast<int>(blockIdx.x % p.p_tiles) * kTileP;
+      int tile = blockIdx.x;
+      for (; g < g_end; ++g) {
+        const int slot = g & (kRawStages - 1);
+        if (!mbar_wait(raw_empty(slot), ((g / kRawStages) & 1) ^ 1, ab)) break;
+        if (s >= p.num_kt) {
+          mbar_arrive(raw_full(slot));   // LoRA stage: nothing to load, keep the phases in step
+        } else {
+          const uint32_t dst = raw_slot(slot);
+          mbar_arrive_expect_tx(raw_full(slot), kAbsTma ? (kTrans ? S::kCodeBytes + 1024 : S::kRawBytes)
+                                                        : S::kCodeBytes);
+          if (!kTrans) {
+            tma_load_2d(dst, &map_code, raw_full(slot), 32 * s, p0);                  // W[p0.., 64s..]
+            if (kAbsTma) tma_load_2d(dst + S::kCodeBytes, &map_abs, raw_full(slot), s & ~3, p0);
+          } else {
+            tma_load_2d(dst, &map_code, raw_full(slot), p0 >> 1, 64 * s);             // W[64s.., p0..]
+            if (kAbsTma) tma_load_2d(dst + S::kCodeBytes, &map_abs, raw_full(slot), (p0 >> 6) & ~3, 64 * s);
+          }
+        }
+        if (++s == total) {
+          s = 0;
+          tile += grid;
+          p0 = (tile % p.p_tiles) * kTileP;
+        }
+      }
+      for (int q = g - 1; q >= 0 && q >= g - kRawStages; --q)
+        mbar_wait(raw_full(q % kRawStages), (q / kRawStages) & 1, ab, false);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -441,39 +543,67 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       // A operand majorness: Y -- W tile K-major, B tile MN-major; dX -- W tile MN-major, A tile K-major
       constexpr uint32_t idesc_w = umma_idesc_bf16(kTileP, BN, kTrans ? 1 : 0, 0);
       constexpr uint32_t idesc_l = umma_idesc_bf16(kTileP, BN, kTrans ? 0 : 1, 0);
-      for (int s = 0; s < total; ++s) {
-        const int slot = s % kMainStages;
-        const uint32_t ph = (s / kMainStages) & 1;
-        if (!mbar_wait(bar0 + 8u * slot, ph, ab)) break;
-        if (!mbar_wait(bar0 + 8u * (kMainStages + slot), ph, ab)) break;
+      int g = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += grid, ++it) {
+        const int acc = it & 1;
+        const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(acc * BN);
+        if (!mbar_wait(tmem_empty(acc), ((it >> 1) & 1) ^ 1, ab)) break;
         tc_fence_after_sync();
-        const uint32_t act = base + slot * S::kStageBytes;
-        const uint32_t wt = act + S::kActBytes;
-        const bool lora = s >= p.num_kt;
+        for (int s = 0; s < total; ++s, ++g) {
+          const int slot = g % kMainStages;
+          const uint32_t ph = (g / kMainStages) & 1;
+          if (!mbar_wait(full_act(slot), ph, ab) || !mbar_wait(full_w(slot), ph, ab)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t act = base + slot * S::kStageBytes;
+          const uint32_t wt = act + S::kActBytes;
+          const bool lora = s >= p.num_kt;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const bool a_mn = (kTrans != lora);
-          const uint64_t ad = a_mn ? sw128_desc(wt + kk * 2048, 8192, 1024) : sw128_desc(wt + kk * 32, 16, 1024);
-          const uint64_t bd = sw128_desc(act + kk * 32, 16, 1024);
-          umma_bf16(tmem_d, ad, bd, lora ? idesc_l : idesc_w, (s | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const bool a_mn = (kTrans != lora);
+            const uint64_t ad = a_mn ? sw128_desc(wt + kk * 2048, 8192, 1024) : sw128_desc(wt + kk * 32, 16, 1024);
+            const uint64_t bd = sw128_desc(act + kk * 32, 16, 1024);
+            umma_bf16(tmem_d, ad, bd, lora ? idesc_l : idesc_w, (s | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty(slot));
         }
-        umma_commit(bar0 + 8u * (2 * kMainStages + slot));
+        if (ok) umma_commit(tmem_full(acc));
       }
-      umma_commit(accum_bar);
+      // every MMA issued by this thread has completed once drain_bar flips
+      umma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, ab, false);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 2 && warp < 10) {
     // ---------------- NF4 dequantisation into the UMMA A operand
     const int dw = warp - 2;                  // 0..7
-    const int grp = dw >> 2;                  // group g converts stages s with s % 2 == g
+    const int grp = dw >> 2;                  // group g converts stages with g % 2 == grp
     const int i = (dw & 3) * 32 + lane;       // operand row written by this thread
     const uint32_t row_off = static_cast<uint32_t>(i) * 128u;
     const uint32_t swz = static_cast<uint32_t>(i & 7);
+    // where this thread's 32 code bytes and absmax sit in a raw slot:
+    //   Y : code row i (32 B, 32-B swizzle), absmax row i, column s % 4
+    //   dX: code row i % 64 (64 B, 64-B swizzle), bytes 32*(i/64).., absmax row i % 64,
+    //       column (p0/64) % 4 + i/64
+    uint32_t code_off[2];
+    if (!kTrans) {
+      const uint32_t x = static_cast<uint32_t>((i >> 2) & 1);
+      code_off[0] = static_cast<uint32_t>(i) * 32u + ((0u ^ x) << 4);
+      code_off[1] = static_cast<uint32_t>(i) * 32u + ((1u ^ x) << 4);
+    } else {
+      const uint32_t nl = static_cast<uint32_t>(i & 63), kbl = static_cast<uint32_t>(i >> 6);
+      const uint32_t x = (nl >> 1) & 3u;
+      code_off[0] = nl * 64u + (((2u * kbl) ^ x) << 4);
+      code_off[1] = nl * 64u + (((2u * kbl + 1u) ^ x) << 4);
+    }
     const int kblocks = p.K >> 6;
-    // absmax index of the 64-element block this thread expands at NF4 stage s
-    // (or -1 outside W): Y uses W rows p0.. along K; dX uses W rows 64s.. and
-    // the two 64-column blocks of this CTA's 128 features.
-    auto block_of = [&](int s) -> int64_t {
+    // absmax straight from global memory when it cannot come by TMA (d_in % 256 != 0)
+    auto absmax_direct = [&](int s, int p0) -> float {
+      if (kAbsTma || s >= p.num_kt) return 0.0f;
       int n, kb;
       if (!kTrans) {
         n = p0 + i;
@@ -482,92 +612,114 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         n = s * 64 + (i & 63);
         kb = (p0 >> 6) + (i >> 6);
       }
-      if (n >= p.N || kb >= kblocks) return -1;
-      return static_cast<int64_t>(n) * kblocks + kb;
+      if (n >= p.N || kb >= kblocks) return 0.0f;
+      return ldg_nc_f32(p.absmax + static_cast<int64_t>(n) * kblocks + kb);
     };
-    const uint8_t* packed = p.packed;
-    const float* absmax = p.absmax;
-
-    // codes and absmax of this thread's block, loaded two of its iterations ahead
-    struct Pending {
-      uint4 lo, hi;
-      float am;
-      bool valid;
+    // stage g = tile_it * total + s; this group takes every other g
+    int s = grp, tile = blockIdx.x;
+    int p0 = (tile % p.p_tiles) * kTileP;
+    auto advance = [&](int& ss, int& tt, int& pp) {
+      ss += 2;
+      while (ss >= total) {
+        ss -= total;
+        tt += grid;
+        pp = (tt % p.p_tiles) * kTileP;
+      }
     };
-    auto fetch = [&](int s) -> Pending {
-      Pending f;
-      f.lo = make_uint4(0u, 0u, 0u, 0u);
-      f.hi = f.lo;
-      f.am = 0.0f;
-      f.valid = false;
-      if (s < p.num_kt) {
-        const int64_t b = block_of(s);
-        if (b >= 0) {
-          f.lo = ldg_nc_v4(packed + 32 * b);
-          f.hi = ldg_nc_v4(packed + 32 * b + 16);
-          f.am = ldg_nc_f32(absmax + b);
-          f.valid = true;
+    int s_next = s, tile_next = tile, p0_next = p0;
+    advance(s_next, tile_next, p0_next);
+    float am_next = (grp < g_end) ? absmax_direct(s, p0) : 0.0f;
+    for (int g = grp; g < g_end; g += 2) {
+      const float am_direct = am_next;
+      am_next = (g + 2 < g_end) ? absmax_direct(s_next, p0_next) : 0.0f;
+      const int slot = g & (kMainStages - 1);
+      const uint32_t ph = (g / kMainStages) & 1;
+      // every lane acquires the TMA-written codes itself (a shuffle does not order memory)
+      if (!__all_sync(0xffffffffu, mbar_wait(raw_full(slot), ph, ab))) break;
+      uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
+      float am = am_direct;
+      const bool nf4 = s < p.num_kt;
+      if (nf4) {
+        const uint32_t rs = raw_slot(slot);
+        c0 = ld_shared_v4(rs + code_off[0]);
+        c1 = ld_shared_v4(rs + code_off[1]);
+        if (kAbsTma) {
+          const int col = !kTrans ? (s & 3) : (((p0 >> 6) & 3) + (i >> 6));
+          const int row = !kTrans ? i : (i & 63);
+          am = ld_shared_f32(rs + S::kCodeBytes + static_cast<uint32_t>(row * 16 + col * 4));
         }
       }
-      return f;
-    };
-    Pending cur = fetch(grp);
-    Pending nxt = fetch(grp + 2);
-    for (int s = grp; s < total; s += 2) {
-      const Pending later = fetch(s + 4);
-      const int slot = s % kMainStages;
-      const uint32_t ph = (s / kMainStages) & 1;
-      // one lane waits for the slot to be free, the warp follows (warp-uniform exit on abort)
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait(bar0 + 8u * (2 * kMainStages + slot), ph ^ 1, ab);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      if (s < p.num_kt) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(raw_empty(slot));
+      if (!__all_sync(0xffffffffu, mbar_wait(empty(slot), ph ^ 1, ab))) break;
+      if (nf4) {
         const uint32_t dst = base + slot * S::kStageBytes + S::kActBytes + row_off;
-        if (cur.valid) {
-          const Nf4BlockTable tab = nf4_block_table(cur.am);
-          const uint32_t words[8] = {cur.lo.x, cur.lo.y, cur.lo.z, cur.lo.w,
-                                     cur.hi.x, cur.hi.y, cur.hi.z, cur.hi.w};
+        const Nf4BlockTable tab = nf4_block_table(am);
+        const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-          for (int c = 0; c < 8; ++c) st_shared_v4(dst + ((c ^ swz) << 4), nf4_expand8(words[c], tab));
-        } else {
-#pragma unroll
-          for (int c = 0; c < 8; ++c) st_shared_v4(dst + (c << 4), make_uint4(0u, 0u, 0u, 0u));
-        }
+        for (int c = 0; c < 8; ++c) st_shared_v4(dst + ((c ^ swz) << 4), nf4_expand8(words[c], tab));
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar0 + 8u * (kMainStages + slot));
-      cur = nxt;
-      nxt = later;
+      if (lane == 0) mbar_arrive(full_w(slot));
+      s = s_next;
+      tile = tile_next;
+      p0 = p0_next;
+      advance(s_next, tile_next, p0_next);
     }
-
-    // ---------------- epilogue: TMEM -> bf16 -> shared staging [BN tokens][128 features] -> TMA store
-    bool ok = mbar_wait(accum_bar, 0, ab, false);
-    tc_fence_after_sync();
-    ok = __all_sync(0xffffffffu, ok && (s_abort == 0));
-    const int quarter = warp & 3;
-    const int half = dw >> 2;
-    const int prow = quarter * 32 + lane;
-    if (ok) {
-      for (int c0 = half * (BN / 2); c0 < (half + 1) * (BN / 2); c0 += 32) {
+  } else if (warp >= 10 && warp < 14) {
+    // ---------------- epilogue: TMEM -> bf16 -> staging -> TMA store
+    // staging: two [32 tokens][64 features] bf16 halves in the 128-B swizzled layout;
+    // lanes pair up (shuffle) so each thread stores two adjacent features of one token.
+    const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
+    const int prow = quarter * 32 + lane;         // output feature within the tile
+    const bool leader = (warp == 10 && lane == 0);
+    const uint32_t staging = base + S::kStagingOffset;
+    const int f_even = prow & ~1;                 // first of the two features this lane stores
+    const uint32_t half_off = static_cast<uint32_t>(f_even >> 6) * 4096u;
+    const uint32_t chunk16 = static_cast<uint32_t>((f_even & 63) >> 3);
+    const uint32_t in16 = static_cast<uint32_t>((f_even & 7) * 2);
+    const bool odd = (lane & 1) != 0;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += grid, ++it) {
+      const int p0 = (tile % p.p_tiles) * kTileP;
+      const int t0 = (tile / p.p_tiles) * BN;
+      const int acc = it & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(tmem_full(acc), (it >> 1) & 1, ab))) break;
+      tc_fence_after_sync();
+      for (int c0 = 0; c0 < BN; c0 += kEpiChunk) {
         uint32_t v[32];
-        tmem_ld32(tmem_d + (static_cast<uint32_t>(quarter * 32) << 16) + c0, v);
+        tmem_ld32(tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16) + c0, v);
         tmem_ld_wait();
+        // the previous chunk's store must have read the staging buffer
+        if (leader) tma_store_wait_read_all();
+        named_bar_sync(1, 128);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[j]));
-          st_shared_u16(base + static_cast<uint32_t>(c0 + j) * (kTileP * 2) + prow * 2,
-                        *reinterpret_cast<const uint16_t*>(&h));
+        for (int jj = 0; jj < kEpiChunk / 2; ++jj) {
+          // tokens a and a + 4: their swizzled rows use disjoint bank groups.
+          // even lane: token a, features (f, f+1); odd lane: token a+4, features (f-1, f)
+          const int a = (jj & 3) + (jj >> 2) * 8;
+          const float mine = __uint_as_float(odd ? v[a + 4] : v[a]);
+          const float give = __uint_as_float(odd ? v[a] : v[a + 4]);
+          const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+          const uint32_t pair = odd ? pack_bf16x2(got, mine) : pack_bf16x2(mine, got);
+          const uint32_t tok = static_cast<uint32_t>(a + (odd ? 4 : 0));
+          st_shared_u32(staging + half_off + tok * 128u + ((chunk16 ^ (tok & 7u)) << 4) + in16, pair);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader && t0 + c0 < p.M) {   // boxes wholly past the last token / feature are not stored
+          tma_store_2d(&map_out, staging, p0, t0 + c0);
+          if (p0 + 64 < (kTrans ? p.K : p.N)) tma_store_2d(&map_out, staging + 4096, p0 + 64, t0 + c0);
+          tma_store_commit();
         }
       }
-      fence_proxy_async_smem();
+      // this accumulator may be overwritten by the MMA of tile it + 2
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tmem_empty(acc));
     }
-    named_bar_sync(1, 256);
-    if (threadIdx.x == 64 && s_abort == 0 && ok) {
-      tma_store_2d(&map_out, base, p0, t0);
-      tma_store_commit();
-      tma_store_wait_all();
-    }
+    if (leader) tma_store_wait_all();
   }
 
   tc_fence_before_sync();
@@ -575,7 +727,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after_sync();
-    tmem_dealloc(tmem_d, BN);
+    tmem_dealloc(tmem_base, 2 * BN);
   }
 }
 
@@ -611,6 +763,19 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* gaddr, uint64_
   return r == CUDA_SUCCESS;
 }
 
+bool make_map_sw(CUtensorMap* m, CUtensorMapDataType dt, const void* gaddr, uint64_t inner,
+                 uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
+                 CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(gaddr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool map_bf16(CUtensorMap* m, const void* g, uint64_t cols, uint64_t rows, uint32_t box_c,
               uint32_t box_r, bool sw) {
   return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, g, cols, rows, cols * 2, box_c, box_r, sw);
@@ -640,10 +805,11 @@ constexpr int skinny_kind(int mode) {
   return mode == kRowsT ? kKindRowsT : mode == kRowsG ? kKindRowsG : kKindRed;
 }
 
-template <int MODE, int RP>
+template <int MODE, int RP, int NSPLIT>
 cudaError_t launch_skinny_rp(const CUtensorMap (&maps)[4], const SkinnyParams& sp, int tiles,
-                             int split, cudaStream_t stream) {
-  auto kern = lora_skinny_kernel<MODE, RP>;
+                             cudaStream_t stream) {
+  constexpr int split = NSPLIT;
+  auto kern = lora_skinny_kernel<MODE, RP, NSPLIT>;
   cudaError_t e = set_smem(kern, SkinnySmem<RP>::kBytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -662,24 +828,45 @@ cudaError_t launch_skinny_rp(const CUtensorMap (&maps)[4], const SkinnyParams& s
   return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], sp);
 }
 
+template <int MODE, int RP>
+cudaError_t launch_skinny_split(const CUtensorMap (&maps)[4], const SkinnyParams& sp, int tiles,
+                                int split, cudaStream_t stream) {
+  switch (split) {
+    case 1: return launch_skinny_rp<MODE, RP, 1>(maps, sp, tiles, stream);
+    case 2: return launch_skinny_rp<MODE, RP, 2>(maps, sp, tiles, stream);
+    case 4: return launch_skinny_rp<MODE, RP, 4>(maps, sp, tiles, stream);
+    default: return launch_skinny_rp<MODE, RP, 8>(maps, sp, tiles, stream);
+  }
+}
+
 template <int MODE>
 cudaError_t launch_skinny(int rp, const CUtensorMap (&maps)[4], const SkinnyParams& sp, int tiles,
                           int split, cudaStream_t stream) {
-  if (rp == 64) return launch_skinny_rp<MODE, 64>(maps, sp, tiles, split, stream);
-  return launch_skinny_rp<MODE, 128>(maps, sp, tiles, split, stream);
+  if (rp == 64) return launch_skinny_split<MODE, 64>(maps, sp, tiles, split, stream);
+  return launch_skinny_split<MODE, 128>(maps, sp, tiles, split, stream);
+}
+
+template <int BN, bool kTrans, bool kAbsTma>
+cudaError_t launch_main_bn(const CUtensorMap (&maps)[6], MainParams mp, int P, int M,
+                           cudaStream_t stream) {
+  auto kern = lora_main_kernel<BN, kTrans, kAbsTma>;
+  cudaError_t e = set_smem(kern, MainSmem<BN>::kBytes);
+  if (e != cudaSuccess) return e;
+  mp.p_tiles = (P + kTileP - 1) / kTileP;
+  mp.t_tiles = (M + BN - 1) / BN;
+  const int tiles = mp.p_tiles * mp.t_tiles;
+  const int grid = std::min(tiles, sm_count());
+  LaunchScope scope(kTrans ? kKindMainDx : kKindMainFwd, stream);
+  kern<<<grid, kMainThreads, MainSmem<BN>::kBytes, stream>>>(maps[0], maps[1], maps[2], maps[3],
+                                                              maps[4], maps[5], mp);
+  return cudaGetLastError();
 }
 
 template <int BN, bool kTrans>
-cudaError_t launch_main_bn(const CUtensorMap& ma, const CUtensorMap& ml, const CUtensorMap& mw,
-                           const CUtensorMap& mo, const MainParams& mp, int P, int M,
-                           cudaStream_t stream) {
-  auto kern = lora_main_kernel<BN, kTrans>;
-  cudaError_t e = set_smem(kern, MainSmem<BN>::kBytes);
-  if (e != cudaSuccess) return e;
-  dim3 grid((P + kTileP - 1) / kTileP, (M + BN - 1) / BN, 1);
-  LaunchScope scope(kTrans ? kKindMainDx : kKindMainFwd, stream);
-  kern<<<grid, kMainThreads, MainSmem<BN>::kBytes, stream>>>(ma, ml, mw, mo, mp);
-  return cudaGetLastError();
+cudaError_t launch_main_abs(const CUtensorMap (&maps)[6], const MainParams& mp, bool abs_tma, int P,
+                            int M, cudaStream_t stream) {
+  if (abs_tma) return launch_main_bn<BN, kTrans, true>(maps, mp, P, M, stream);
+  return launch_main_bn<BN, kTrans, false>(maps, mp, P, M, stream);
 }
 
 int pick_bn(int M) { return M <= 64 ? 64 : (M <= 128 ? 128 : 256); }
@@ -706,23 +893,34 @@ cudaError_t launch_main(const LayerDims& d, const uint16_t* act, const uint16_t*
   const int P = kTrans ? d.K : d.N;     // output features
   const int C = kTrans ? d.N : d.K;     // contraction length of the NF4 part
   const int bn = pick_bn(d.M);
-  CUtensorMap ma, ml, mw, mo;
-  bool ok = map_bf16(&ma, act, C, d.M, 64, bn, true) && map_bf16(&ml, lact, d.rp, d.M, 64, bn, true) &&
-            map_bf16(&mo, out, P, d.M, kTileP, bn, false);
-  if (kTrans) ok = ok && map_bf16(&mw, lw, lw_cols, d.K, 64, kTileP, true);   // A [K, r]
-  else ok = ok && map_bf16(&mw, lw, d.N, d.r, 64, 64, true);                   // B [r, N]
+  const bool abs_tma = (d.K % 256) == 0;   // absmax rows are 16-byte multiples
+  CUtensorMap maps[6];
+  bool ok = map_bf16(&maps[0], act, C, d.M, 64, bn, true) && map_bf16(&maps[1], lact, d.rp, d.M, 64, bn, true) &&
+            make_map(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, P, d.M, static_cast<uint64_t>(P) * 2, 64,
+                     kEpiChunk, true);
+  if (kTrans) ok = ok && map_bf16(&maps[2], lw, lw_cols, d.K, 64, kTileP, true);   // A [K, r]
+  else ok = ok && map_bf16(&maps[2], lw, d.N, d.r, 64, 64, true);                   // B [r, N]
+  // NF4 codes as bytes [N, K/2]; absmax as fp32 [N, K/64]
+  ok = ok && make_map_sw(&maps[4], CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, d.K / 2, d.N, d.K / 2,
+                         kTrans ? 64 : 32, kTrans ? 64 : kTileP,
+                         kTrans ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
+  if (abs_tma)
+    ok = ok && make_map_sw(&maps[5], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, absmax, d.K / 64, d.N, d.K / 16, 4,
+                           kTrans ? 64 : kTileP, CU_TENSOR_MAP_SWIZZLE_NONE);
+  else
+    maps[5] = maps[4];
   if (!ok) return cudaErrorInvalidValue;
   MainParams mp;
-  mp.packed = packed;
   mp.absmax = absmax;
+  mp.M = d.M;
   mp.K = d.K;
   mp.N = d.N;
   mp.num_kt = (C + kTileK - 1) / kTileK;
   mp.num_lt = d.rp / kTileK;
   mp.status = status;
-  if (bn == 64) return launch_main_bn<64, kTrans>(ma, ml, mw, mo, mp, P, d.M, stream);
-  if (bn == 128) return launch_main_bn<128, kTrans>(ma, ml, mw, mo, mp, P, d.M, stream);
-  return launch_main_bn<256, kTrans>(ma, ml, mw, mo, mp, P, d.M, stream);
+  if (bn == 64) return launch_main_abs<64, kTrans>(maps, mp, abs_tma, P, d.M, stream);
+  if (bn == 128) return launch_main_abs<128, kTrans>(maps, mp, abs_tma, P, d.M, stream);
+  return launch_main_abs<256, kTrans>(maps, mp, abs_tma, P, d.M, stream);
 }
 
 // Pads A to [K, rp] (only needed when r % 8 != 0).

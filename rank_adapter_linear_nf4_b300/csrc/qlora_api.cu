@@ -6,7 +6,7 @@
 #include <vector>
 #include <cuda_runtime.h>
 
-#include "../../include/qlora.h"
+#include "qlora.h"
 #include "kernels.h"
 
 namespace {
