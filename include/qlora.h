@@ -145,6 +145,32 @@ qlora_status qlora_linear_fwd(const uint16_t* X, int64_t M, int64_t d_in, int64_
                               qlora_stream_t stream);
 
 /*
+ * Forward that allocates nothing: the same computation and outputs as
+ * qlora_linear_fwd, without the workspace arguments.  (An interface addition
+ * of this library; the Unsloth pages have no counterpart.)
+ *
+ * For callers that cannot hand the layer a workspace: a process whose device
+ * memory belongs to another allocator, a loop that must not allocate after
+ * start-up, or glue code that only holds the layer's own tensors.  Its
+ * scratch is a fixed 8 MiB device array inside this library, which every GPU
+ * that loads the library keeps for the life of the process.
+ *   - Needs (d_in + M) * rp * 2 bytes of that array, rp = 64 * ceil(r / 64)
+ *     (each part rounded up to 1 KiB); larger shapes return
+ *     QLORA_ERR_WORKSPACE and launch nothing.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the array: calls whose GPU work overlaps (other
+ *     streams, unordered threads) race on it.  Everything a call reads from
+ *     it is written earlier in the same call, so nothing needs clearing.
+ * Other arguments, requirements and errors as qlora_linear_fwd.
+ */
+qlora_status qlora_linear_fwd_noalloc(const uint16_t* X, int64_t M, int64_t d_in, int64_t d_out,
+                                      const uint8_t* packed, const float* absmax,
+                                      const uint16_t* A, const uint16_t* B, int32_t r, float s,
+                                      uint16_t* Y, float* XA_save, qlora_stream_t stream);
+
+/*
  * Backward (the hand-written gradients; W is frozen, so there is no dW):
  *   G  = dY . B^T
  *   dX = dY . W_deq + s . G . A^T      [M, d_in]  bf16, written; may be NULL to skip

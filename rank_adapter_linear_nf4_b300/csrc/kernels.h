@@ -31,6 +31,13 @@ struct LaunchScope {
   int slot;
 };
 
+// Device address of the library's status word on the current device (nullptr
+// on failure; *cuda_error then holds the cudaError_t value).
+int* device_status_word(int* cuda_error);
+
+// Makes qlora_last_cuda_error() report `cuda_error` on the calling thread.
+void record_cuda_error(int cuda_error);
+
 // NF4 codec (nf4_codec.cu).
 cudaError_t launch_quantize_nf4(const uint16_t* W, int64_t n_elems, uint8_t* packed, float* absmax,
                                 cudaStream_t stream);

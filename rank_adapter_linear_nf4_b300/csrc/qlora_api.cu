@@ -103,6 +103,15 @@ cudaEvent_t take_event() {
 
 namespace qlora {
 
+void record_cuda_error(int cuda_error) { g_last_cuda_error = cuda_error; }
+
+int* device_status_word(int* cuda_error) {
+  int* word = nullptr;
+  const qlora_status st = status_word(&word);
+  if (cuda_error != nullptr) *cuda_error = (st == QLORA_OK) ? 0 : g_last_cuda_error;
+  return st == QLORA_OK ? word : nullptr;
+}
+
 LaunchScope::LaunchScope(int k, cudaStream_t s) : kind(k), stream(s), slot(-1) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (!g_profiling.load(std::memory_order_relaxed)) return;

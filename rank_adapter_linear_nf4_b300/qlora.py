@@ -39,6 +39,9 @@ _SIGNATURES = {
     "qlora_linear_fwd": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p,
                                         _c_void_p, _c_void_p, _i32, _f32, _c_void_p, _c_void_p,
                                         _c_void_p, _sz, _c_void_p]),
+    "qlora_linear_fwd_noalloc": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p,
+                                                _c_void_p, _c_void_p, _i32, _f32, _c_void_p, _c_void_p,
+                                                _c_void_p]),
     "qlora_linear_bwd": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p,
                                         _c_void_p, _c_void_p, _c_void_p, _i32, _f32, _c_void_p,
                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p, _sz,
@@ -188,6 +191,28 @@ def qlora_linear_fwd(X: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor
         _dev(B, "B", torch.bfloat16), r, float(s), _dev(Y, "Y", torch.bfloat16),
         _dev(XA, "XA", torch.float32), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), _stream(X)))
+    return Y, XA
+
+
+def qlora_linear_fwd_noalloc(X: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor,
+                             A: torch.Tensor, B: torch.Tensor, s: float, *,
+                             Y: torch.Tensor | None = None, XA: torch.Tensor | None = None):
+    """The forward without a workspace: its scratch is a fixed array inside the
+    library (for callers that cannot allocate one).  Returns (Y, XA)."""
+    lib = load_library()
+    M, d_in = X.shape
+    r, d_out = B.shape
+    if A.shape != (d_in, r):
+        raise ValueError(f"A must be [{d_in}, {r}], got {tuple(A.shape)}")
+    if Y is None:
+        Y = torch.empty(M, d_out, dtype=torch.bfloat16, device=X.device)
+    if XA is None:
+        XA = torch.empty(M, r, dtype=torch.float32, device=X.device)
+    _check("qlora_linear_fwd_noalloc", lib.qlora_linear_fwd_noalloc(
+        _dev(X, "X", torch.bfloat16), M, d_in, d_out, _dev(packed, "packed", torch.uint8),
+        _dev(absmax, "absmax", torch.float32), _dev(A, "A", torch.bfloat16),
+        _dev(B, "B", torch.bfloat16), r, float(s), _dev(Y, "Y", torch.bfloat16),
+        _dev(XA, "XA", torch.float32), _stream(X)))
     return Y, XA
 
 
