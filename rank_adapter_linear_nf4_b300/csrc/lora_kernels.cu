@@ -159,6 +159,9 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   Abort ab{&s_abort, p.status};
 
   if (threadIdx.x == 0) {
+    // a dependent kernel may be scheduled now: it waits (griddepcontrol.wait)
+    // before it reads anything this kernel writes
+    griddep_launch_dependents();
     s_abort = 0;
     for (int i = 0; i < S::kStages; ++i) {
       mbar_init(bar0 + 8u * i, 1);                    // full
@@ -347,6 +350,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
   // nobody leaves while a peer may still read its shared memory
   cluster_sync_all();
+  // when launched with programmatic serialisation this kernel may overlap the one
+  // before it; finishing only after that one has finished keeps the stream order
+  // seen by later work (a later normal launch waits for this kernel alone)
+  griddep_wait();
   tc_fence_before_sync();
   __syncthreads();
   if (warp == 1) {
@@ -472,6 +479,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       int s = 0, p0 = static_cast<int>(blockIdx.x % p.p_tiles) * kTileP;
       int t0 = static_cast<int>(blockIdx.x / p.p_tiles) * BN;
       int tile = blockIdx.x;
+      bool lora_ready = false;
       for (; g < g_end; ++g) {
         const int slot = g & (kMainStages - 1);
         if (!mbar_wait(empty(slot), ((g / kMainStages) & 1) ^ 1, ab)) break;
@@ -480,6 +488,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           mbar_arrive_expect_tx(full_act(slot), S::kActBytes);
           tma_load_2d(act, &map_act, full_act(slot), s * kTileK, t0);
         } else {
+          if (!lora_ready) {
+            // the low-rank activations come from the previous kernel: wait for it
+            // here (the NF4 stages before this point only read the call's inputs),
+            // then let the next kernel start on SMs this grid frees.
+            griddep_wait();
+            griddep_launch_dependents();
+            lora_ready = true;
+          }
           const int j = s - p.num_kt;
           mbar_arrive_expect_tx(full_act(slot), S::kActBytes + S::kWBytes);
           tma_load_2d(act, &map_lact, full_act(slot), j * kTileK, t0);
@@ -649,8 +665,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           am = ld_shared_f32(rs + S::kCodeBytes + static_cast<uint32_t>(row * 16 + col * 4));
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(raw_empty(slot));
       if (!__all_sync(0xffffffffu, mbar_wait(empty(slot), ph ^ 1, ab))) break;
       if (nf4) {
         const uint32_t dst = base + slot * S::kStageBytes + S::kActBytes + row_off;
@@ -662,6 +676,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(full_w(slot));
+      // release the code slot only now: the codes have been consumed, so the loads
+      // that read them have completed.  Released right after issuing the loads, the
+      // TMA refill of the slot could land before a lane's load had read it.
+      if (lane == 0) mbar_arrive(raw_empty(slot));
       s = s_next;
       tile = tile_next;
       p0 = p0_next;
@@ -807,7 +825,7 @@ constexpr int skinny_kind(int mode) {
 
 template <int MODE, int RP, int NSPLIT>
 cudaError_t launch_skinny_rp(const CUtensorMap (&maps)[4], const SkinnyParams& sp, int tiles,
-                             cudaStream_t stream) {
+                             bool pdl, cudaStream_t stream) {
   constexpr int split = NSPLIT;
   auto kern = lora_skinny_kernel<MODE, RP, NSPLIT>;
   cudaError_t e = set_smem(kern, SkinnySmem<RP>::kBytes);
@@ -817,33 +835,37 @@ cudaError_t launch_skinny_rp(const CUtensorMap (&maps)[4], const SkinnyParams& s
   cfg.blockDim = dim3(kSkThreads, 1, 1);
   cfg.dynamicSmemBytes = SkinnySmem<RP>::kBytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = split;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   LaunchScope scope(skinny_kind(MODE), stream);
   return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], sp);
 }
 
 template <int MODE, int RP>
 cudaError_t launch_skinny_split(const CUtensorMap (&maps)[4], const SkinnyParams& sp, int tiles,
-                                int split, cudaStream_t stream) {
+                                int split, bool pdl, cudaStream_t stream) {
   switch (split) {
-    case 1: return launch_skinny_rp<MODE, RP, 1>(maps, sp, tiles, stream);
-    case 2: return launch_skinny_rp<MODE, RP, 2>(maps, sp, tiles, stream);
-    case 4: return launch_skinny_rp<MODE, RP, 4>(maps, sp, tiles, stream);
-    default: return launch_skinny_rp<MODE, RP, 8>(maps, sp, tiles, stream);
+    case 1: return launch_skinny_rp<MODE, RP, 1>(maps, sp, tiles, pdl, stream);
+    case 2: return launch_skinny_rp<MODE, RP, 2>(maps, sp, tiles, pdl, stream);
+    case 4: return launch_skinny_rp<MODE, RP, 4>(maps, sp, tiles, pdl, stream);
+    default: return launch_skinny_rp<MODE, RP, 8>(maps, sp, tiles, pdl, stream);
   }
 }
 
+// `pdl`: launched with programmatic serialisation -- only for a kernel whose
+// inputs were complete before the previous kernel on the stream started.
 template <int MODE>
 cudaError_t launch_skinny(int rp, const CUtensorMap (&maps)[4], const SkinnyParams& sp, int tiles,
-                          int split, cudaStream_t stream) {
-  if (rp == 64) return launch_skinny_split<MODE, 64>(maps, sp, tiles, split, stream);
-  return launch_skinny_split<MODE, 128>(maps, sp, tiles, split, stream);
+                          int split, cudaStream_t stream, bool pdl = false) {
+  if (rp == 64) return launch_skinny_split<MODE, 64>(maps, sp, tiles, split, pdl, stream);
+  return launch_skinny_split<MODE, 128>(maps, sp, tiles, split, pdl, stream);
 }
 
 template <int BN, bool kTrans, bool kAbsTma>
@@ -855,11 +877,20 @@ cudaError_t launch_main_bn(const CUtensorMap (&maps)[6], MainParams mp, int P, i
   mp.p_tiles = (P + kTileP - 1) / kTileP;
   mp.t_tiles = (M + BN - 1) / BN;
   const int tiles = mp.p_tiles * mp.t_tiles;
-  const int grid = std::min(tiles, sm_count());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(std::min(tiles, sm_count()), 1, 1);
+  cfg.blockDim = dim3(kMainThreads, 1, 1);
+  cfg.dynamicSmemBytes = MainSmem<BN>::kBytes;
+  cfg.stream = stream;
+  // programmatic serialisation: the NF4 stages start while the low-rank kernel
+  // before this one finishes; the producer waits for it before the LoRA stages
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   LaunchScope scope(kTrans ? kKindMainDx : kKindMainFwd, stream);
-  kern<<<grid, kMainThreads, MainSmem<BN>::kBytes, stream>>>(maps[0], maps[1], maps[2], maps[3],
-                                                              maps[4], maps[5], mp);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], mp);
 }
 
 template <int BN, bool kTrans>
@@ -1022,6 +1053,13 @@ cudaError_t run_backward(const LayerDims& d, const uint16_t* X, const uint16_t* 
     e = launch_skinny<kRowsG>(d.rp, maps, sp, tiles, pick_split(tiles, sp.num_ct), stream);
     if (e != cudaSuccess) return e;
   }
+  // dX first; the dA/dB kernel then runs in the SMs dX's last tiles leave idle.  It may start
+  // before dX finishes because dX lets it go only after its own wait on the G kernel.
+  const bool with_dx = dX != nullptr;
+  if (with_dx) {
+    e = launch_main<true>(d, dY, ws.s_g, la.ptr, la.cols, dX, packed, absmax, status, stream);
+    if (e != cudaSuccess) return e;
+  }
   // dA = X^T . bf16(s*G)  -> [K, r]   and   dB = bf16(s*T)^T . dY  -> [r, N], one launch
   {
     CUtensorMap maps[4];
@@ -1039,11 +1077,10 @@ cudaError_t run_backward(const LayerDims& d, const uint16_t* X, const uint16_t* 
     sp.job[1].out_f32 = dB;
     sp.status = status;
     const int tiles = sp.job[0].tiles + sp.job[1].tiles;
-    e = launch_skinny<kRed>(d.rp, maps, sp, tiles, pick_split(tiles, sp.num_ct), stream);
+    e = launch_skinny<kRed>(d.rp, maps, sp, tiles, pick_split(tiles, sp.num_ct), stream, with_dx);
     if (e != cudaSuccess) return e;
   }
-  if (dX == nullptr) return cudaSuccess;
-  return launch_main<true>(d, dY, ws.s_g, la.ptr, la.cols, dX, packed, absmax, status, stream);
+  return cudaSuccess;
 }
 
 }  // namespace qlora

@@ -123,6 +123,21 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Blocks until the grids this one depends on (the previous kernel on the
+// stream, when launched with programmatic serialisation) have completed and
+// their memory is visible.  Returns at once for a normally launched kernel.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next kernel on the stream (launched with programmatic
+// serialisation) be scheduled once every CTA of this grid has signalled or exited.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- cluster
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
