@@ -35,12 +35,43 @@ def shape_of(name):
     return synthetic.SHAPES[name]
 
 
+def fwd_only(sh) -> bool:
+    """Small-token workloads (M < 128) are forward passes: weight-streaming, HBM-bound."""
+    return sh.M < 128
+
+
 def step_flops(sh) -> float:
-    """Algorithmic flops of one forward + backward (no dW: the base is frozen)."""
+    """Algorithmic flops of one step: forward + backward (no dW: the base is
+    frozen), or the forward alone for the small-token workloads."""
     M, K, N, r = sh.M, sh.d_in, sh.d_out, sh.r
     fwd = 2 * M * K * N + 2 * M * r * (K + N)
     bwd = 2 * M * K * N + 4 * M * r * (K + N)
-    return float(fwd + bwd)
+    return float(fwd if fwd_only(sh) else fwd + bwd)
+
+
+def sources_hash() -> str:
+    """Hash of the CUDA sources: a stored ncu traffic figure counts only for these."""
+    import hashlib
+    h = hashlib.sha1()
+    csrc = os.path.join(ROOT, "rank_adapter_linear_nf4_b300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from profiles/traffic.json, if captured from these sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(f"{kernel}@{workload}")
+    if not e or e.get("sources") != sources_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
 
 
 def kernel_work(sh, kind):
@@ -55,7 +86,7 @@ def kernel_work(sh, kind):
 def workload_desc(sh) -> str:
     kind = "rank-stabilised " if sh.rank_stabilised else ""
     return (f"{sh.name}: M={sh.M} tokens, d_in={sh.d_in} -> d_out={sh.d_out}, r={sh.r}, "
-            f"{kind}s={sh.s:g}, NF4 blocksize 64, fwd+bwd")
+            f"{kind}s={sh.s:g}, NF4 blocksize 64, {'fwd' if fwd_only(sh) else 'fwd+bwd'}")
 
 
 def load_peaks():
@@ -300,12 +331,15 @@ def run_ours(args):
                          dB=torch.empty(r, N, dtype=torch.float32, device=dev)))
     torch.cuda.synchronize()
 
+    only_fwd = fwd_only(sh)
+
     def step(i):
         t = sets[i % n_sets]
         qlora.qlora_linear_fwd(t["X"], t["packed"], t["absmax"], t["A"], t["B"], sh.s,
                                Y=t["Y"], XA=t["XA"], workspace=ws)
-        qlora.qlora_linear_bwd(t["X"], t["dY"], t["packed"], t["absmax"], t["A"], t["B"], sh.s, t["XA"],
-                               dX=t["dX"], dA=t["dA"], dB=t["dB"], workspace=ws)
+        if not only_fwd:
+            qlora.qlora_linear_bwd(t["X"], t["dY"], t["packed"], t["absmax"], t["A"], t["B"], sh.s,
+                                   t["XA"], dX=t["dX"], dA=t["dA"], dB=t["dB"], workspace=ws)
 
     def timed(fn, steps):
         start = torch.cuda.Event(enable_timing=True)
@@ -372,6 +406,10 @@ def run_ours(args):
     roofline["flops_per_launch"] = kf
     roofline["algorithmic_bytes_per_launch"] = kb
     roofline["avg_launch_us"] = k_avg_s * 1e6
+    roofline["traffic"] = stored_traffic(roof_kind, sh.name)
+    roofline["traffic_note"] = ("dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed ncu "
+                                "capture of these kernel sources" if roofline["traffic"] is not None else
+                                "no ncu capture of the current kernel sources")
     per_kernel = {k: {"launches": n, "total_ms": round(t, 4), "avg_us": round(t / n * 1e3, 2),
                       "share": round(t / sum(v[0] for v in kernels.values()), 4)}
                   for k, (t, n) in sorted(kernels.items(), key=lambda kv: -kv[1][0])}
@@ -388,21 +426,25 @@ def run_ours(args):
 
     def e2e_step(i):
         dX_in.copy_(hX, non_blocking=True)
-        dY_in.copy_(hdY, non_blocking=True)
+        if not only_fwd:
+            dY_in.copy_(hdY, non_blocking=True)
         qlora.qlora_linear_fwd(dX_in, t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
                                Y=t0["Y"], XA=t0["XA"], workspace=ws)
-        qlora.qlora_linear_bwd(dX_in, dY_in, t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
-                               t0["XA"], dX=t0["dX"], dA=t0["dA"], dB=t0["dB"], workspace=ws)
         hY.copy_(t0["Y"], non_blocking=True)
-        hdX.copy_(t0["dX"], non_blocking=True)
-        hdA.copy_(t0["dA"], non_blocking=True)
-        hdB.copy_(t0["dB"], non_blocking=True)
+        if not only_fwd:
+            qlora.qlora_linear_bwd(dX_in, dY_in, t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
+                                   t0["XA"], dX=t0["dX"], dA=t0["dA"], dB=t0["dB"], workspace=ws)
+            hdX.copy_(t0["dX"], non_blocking=True)
+            hdA.copy_(t0["dA"], non_blocking=True)
+            hdB.copy_(t0["dB"], non_blocking=True)
 
     e2e_step(0)
     e2e_steps = max(3, min(args.steps, 200))
     e2e_ms = timed(e2e_step, e2e_steps) / e2e_steps
-    h2d = hX.numel() * 2 + hdY.numel() * 2
-    d2h = hY.numel() * 2 + hdX.numel() * 2 + hdA.numel() * 4 + hdB.numel() * 4
+    h2d = hX.numel() * 2 + (0 if only_fwd else hdY.numel() * 2)
+    d2h = hY.numel() * 2 + (0 if only_fwd else hdX.numel() * 2 + hdA.numel() * 4 + hdB.numel() * 4)
+
+    codec = codec_rooflines(sh, sets, dev, peaks, stream)
 
     if rank != 0:
         if world > 1:
@@ -425,6 +467,7 @@ def run_ours(args):
         "kernels": per_kernel,
         "profiled_ms_per_step": prof_total_ms / args.steps,
         "gpu_launches": launches,
+        "nf4_codec": codec,
         "clocks": clocks,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -435,6 +478,41 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def codec_rooflines(sh, sets, dev, peaks, stream, reps=20):
+    """NF4 quantise and dequantise of this workload's weight (rows a1, a2), timed
+    alone with CUDA events, alternating two weights (> L2 together); HBM-bound."""
+    import torch
+    from rank_adapter_linear_nf4_b300 import qlora
+    n = sh.d_in * sh.d_out
+    Ws = [qlora.qlora_dequant_nf4(t["packed"], t["absmax"], sh.d_out, sh.d_in) for t in sets[:2]]
+    outs = [torch.empty_like(w) for w in Ws]
+    pk = [torch.empty_like(t["packed"]) for t in sets[:2]]
+    am = [torch.empty_like(t["absmax"]) for t in sets[:2]]
+    res = {}
+    for name, fn, nbytes in (
+            ("nf4_quantize", lambda i: qlora.qlora_quantize_nf4(Ws[i % 2], packed=pk[i % 2], absmax=am[i % 2]),
+             2.0 * n + 0.5 * n + n / 16.0),
+            ("nf4_dequant", lambda i: qlora.qlora_dequant_nf4(sets[i % 2]["packed"], sets[i % 2]["absmax"],
+                                                              sh.d_out, sh.d_in, out=outs[i % 2]),
+             0.5 * n + n / 16.0 + 2.0 * n)):
+        for i in range(3):
+            fn(i)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for i in range(reps):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) / reps * 1e3
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[name] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm"], "avg_launch_us": us,
+                     "algorithmic_bytes_per_launch": nbytes, "elements": n}
+    return res
 
 
 def main():
