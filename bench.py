@@ -499,15 +499,17 @@ def codec_rooflines(sh, sets, dev, peaks, stream, reps=20):
              0.5 * n + n / 16.0 + 2.0 * n)):
         for i in range(3):
             fn(i)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
-        a.record(stream)
+        # per-launch CUDA events recorded by the library around each kernel on its
+        # stream: device time of the kernel alone, without host call overhead
+        qlora.qlora_profile_enable(True)
+        qlora.qlora_profile_collect()
         for i in range(reps):
             fn(i)
-        b.record(stream)
-        torch.cuda.synchronize()
-        us = a.elapsed_time(b) / reps * 1e3
+        prof = qlora.qlora_profile_collect()
+        qlora.qlora_profile_enable(False)
+        ms, cnt = prof[name]
+        us = ms / cnt * 1e3
         gbs = nbytes / (us * 1e-6) / 1e9
         res[name] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm"], "avg_launch_us": us,

@@ -72,10 +72,19 @@ __global__ void __launch_bounds__(256) nf4_quantize_kernel(const uint4* __restri
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const float x = __fdiv_rn(w[i], m);
-      uint32_t c = 0;
+      // q = number of thresholds <= x, found by a branch-free binary search:
+      // the thresholds are ascending, so each level halves the candidate range.
+      const bool b3 = x >= th.t[7];
+      const float t2 = b3 ? th.t[11] : th.t[3];
+      const bool b2 = x >= t2;
+      const float t1 = b3 ? (b2 ? th.t[13] : th.t[9]) : (b2 ? th.t[5] : th.t[1]);
+      const bool b1 = x >= t1;
+      const uint32_t hi3 = (b3 ? 8u : 0u) | (b2 ? 4u : 0u) | (b1 ? 2u : 0u);   // 0,2,..,14
+      // last level: threshold t[hi3] (t[14] when hi3 == 14)
+      float t0 = th.t[0];
 #pragma unroll
-      for (int k = 0; k < 15; ++k) c += (x >= th.t[k]) ? 1u : 0u;
-      q[i] = c;
+      for (int k = 2; k <= 14; k += 2) t0 = (hi3 == static_cast<uint32_t>(k)) ? th.t[k] : t0;
+      q[i] = hi3 + ((x >= t0) ? 1u : 0u);
     }
   }
   uint32_t word = 0;
