@@ -60,8 +60,15 @@ struct Workspace {
   uint16_t* a_pad;   // [K, rp]  A with zero columns r..rp-1 (used when r % 8 != 0)
   uint16_t* s_t;     // [M, rp]  bf16(s * X.A), zero-padded
   uint16_t* s_g;     // [M, rp]  bf16(s * dY.B^T), zero-padded
+  // Split-remainder buffers of the main kernel (nullptr: whole tiles only).
+  int* counters;         // pieces finished per split tile, zeroed by the rank-r kernel before it
+  int counter_cap;
+  float* partials;       // fp32 partial tiles
+  size_t partial_bytes;
 };
 size_t workspace_bytes(const LayerDims& d);
+// Bytes of partial tiles the main kernel uses at most for these dimensions.
+size_t split_partial_bytes(const LayerDims& d);
 Workspace carve_workspace(const LayerDims& d, void* base);
 
 cudaError_t run_forward(const LayerDims& d, const uint16_t* X, const uint8_t* packed,

@@ -99,6 +99,8 @@ struct SkinnyParams {
   SkinnyJob job[2];    // kRed: job 0 = dA, job 1 = dB; the rows modes use job 0
   const float* xa;     // kRowsG: saved T [rows, r]
   uint16_t* s_t;       // kRowsG: bf16(s*T) [rows, RP] written from xa
+  int* zero;           // rows modes: split-tile counters of the main kernel that follows
+  int n_zero;
   int* status;
 };
 
@@ -158,6 +160,11 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const int nct = ct_end - ct_begin;
   Abort ab{&s_abort, p.status};
 
+  if (MODE != kRed && blockIdx.x == 0 && blockIdx.y == 0) {
+    // the main kernel after this one counts finished pieces of its split tiles
+    // from zero; it reads the counters only after waiting for this kernel
+    for (int i = static_cast<int>(threadIdx.x); i < p.n_zero; i += kSkThreads) p.zero[i] = 0;
+  }
   if (threadIdx.x == 0) {
     // a dependent kernel may be scheduled now: it waits (griddepcontrol.wait)
     // before it reads anything this kernel writes
@@ -365,31 +372,51 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
 // ============================================================== main fused GEMM
 
-constexpr int kMainStages = 4;       // X / W operand stages
-constexpr int kRawStages = 4;        // NF4 code + absmax stages (TMA); same count, so stage g uses slot g % 4 in both
 constexpr int kEpiChunk = 32;        // tokens per epilogue store
+constexpr int kMinSkStages = 16;     // fewest stages a CTA takes in the split remainder
 // warp 0: TMA for the token operand; warp 1: MMA; warps 2-9: dequant; warps 10-13: epilogue;
 // warp 14: TMA for the NF4 codes and absmax (its own ring, so code latency never holds up operand loads)
 constexpr int kMainThreads = 480;
 
+// Ring depths, as deep as shared memory allows.  With few tokens per tile the
+// kernel streams the weight, and each stage is short: the operand ring must
+// cover a TMA load plus an MMA round trip, the code ring the HBM latency.
+constexpr int main_stages(int bn) { return bn <= 64 ? 8 : 4; }
+constexpr int raw_stages(int bn) { return (bn == 32 || bn == 128) ? 8 : 4; }
+
 template <int BN>
 struct MainSmem {
+  static constexpr int kStages = main_stages(BN);
+  static constexpr int kRaw = raw_stages(BN);
   static constexpr int kActBytes = BN * 128;      // BN tokens x 64 contraction
   static constexpr int kWBytes = kTileP * 128;    // 128 features x 64 contraction
   static constexpr int kStageBytes = kActBytes + kWBytes;
   static constexpr int kCodeBytes = 4096;         // Y: 128 rows x 32 B; dX: 64 rows x 64 B
   static constexpr int kAbsBytes = 2048;          // Y: 128 rows x 4 fp32; dX: 64 rows x 4 fp32
   static constexpr int kRawBytes = kCodeBytes + kAbsBytes;
-  static constexpr int kRawOffset = kMainStages * kStageBytes;
+  static constexpr int kRawOffset = kStages * kStageBytes;
   static constexpr int kChunkBytes = kEpiChunk * kTileP * 2;   // two [32 tokens][64 features] halves
-  static constexpr int kStagingOffset = kRawOffset + kRawStages * kRawBytes;
+  static constexpr int kStagingOffset = kRawOffset + kRaw * kRawBytes;
   static constexpr int kBarOffset = kStagingOffset + kChunkBytes;
-  static constexpr int kBytes = kBarOffset + 256 + 1024;
+  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kRaw + 5);
+  static constexpr int kBytes = kBarOffset + 512 + 1024;
+  static_assert(kBarBytes <= 512, "barrier area");
   static_assert(kBytes <= 232448, "shared memory budget");
 };
 
+// Work schedule of the persistent grid.  Tiles (128 features x BN tokens,
+// tile id = token_tile * p_tiles + feature_tile) are cut into stages: the NF4
+// stages of the contraction, then the LoRA stages.
+//   * whole tiles: CTA c takes tiles c, c + grid, ... below dp_tiles;
+//   * split remainder: the stages of tiles dp_tiles.. are laid end to end and
+//     cut into sk_ctas equal ranges, one per CTA 0..sk_ctas-1.  A range covers
+//     pieces of one or more tiles; a piece that is not a whole tile writes an
+//     fp32 partial tile, and the last piece of a tile to finish (a per-tile
+//     counter) adds the partials in contraction order and stores the tile.
 struct MainParams {
   const float* absmax;     // [N * K / 64], read directly when kAbsTma is false
+  float* partials;         // [2 * sk_ctas][BN][128] fp32 partial tiles (split remainder only)
+  int* counters;           // [sk_tiles] pieces finished per split tile; zero at launch
   int M;                   // tokens
   int K;                   // d_in
   int N;                   // d_out
@@ -397,14 +424,98 @@ struct MainParams {
   int num_lt;              // LoRA stages per tile
   int p_tiles;             // output-feature tiles of 128
   int t_tiles;             // token tiles of BN
+  int dp_tiles;            // tiles taken whole, round robin
+  int dp_rounds;           // ceil(dp_tiles / grid)
+  int sk_tiles;            // tiles dp_tiles .. dp_tiles + sk_tiles - 1 are split
+  int sk_ctas;             // CTAs sharing the split remainder
   int* status;
 };
 
-// Persistent: CTA c takes tiles c, c + gridDim.x, ...; tile id = token_tile * p_tiles + feature_tile.
-// Two TMEM accumulators let the epilogue of one tile overlap the main loop of the next.
-// NF4 codes (and, when kAbsTma, the absmax values) of each stage arrive by TMA in a
-// ring of their own; TMA zero-fills rows and columns outside W, so outside W the
-// dequantised operand is zero without per-thread bounds checks.
+// Piece `idx` of this CTA's work: tile and stage range [sb, se).  Order: the
+// first whole-tile round, then the split pieces, then the other whole-tile
+// rounds -- the pieces' fixups then overlap the main loop of later tiles, and
+// the LoRA stages in the pieces find the previous kernel finished.
+__device__ __forceinline__ bool main_piece(const MainParams& p, int cta, int grid, int idx, int& tile,
+                                           int& sb, int& se) {
+  const int total = p.num_kt + p.num_lt;
+  const int dp_first = p.dp_rounds > 0 ? 1 : 0;
+  int n_sk = 0;
+  int64_t lo = 0, hi = 0;
+  if (cta < p.sk_ctas) {
+    const int64_t len = static_cast<int64_t>(p.sk_tiles) * total;
+    lo = len * cta / p.sk_ctas;
+    hi = len * (cta + 1) / p.sk_ctas;
+    if (lo < hi) n_sk = static_cast<int>((hi - 1) / total - lo / total) + 1;
+  }
+  if (idx >= dp_first && idx < dp_first + n_sk) {
+    const int j = static_cast<int>(lo / total) + (idx - dp_first);
+    tile = p.dp_tiles + j;
+    sb = static_cast<int>(max(lo - static_cast<int64_t>(j) * total, int64_t(0)));
+    se = static_cast<int>(min(hi - static_cast<int64_t>(j) * total, static_cast<int64_t>(total)));
+    return true;
+  }
+  const int round = idx < dp_first ? 0 : idx - n_sk;
+  if (round >= p.dp_rounds) return false;
+  tile = cta + round * grid;
+  sb = 0;
+  se = total;
+  // with a split remainder every CTA has exactly dp_rounds whole tiles; without
+  // one, the last round may be short
+  return tile < p.dp_tiles;
+}
+
+// The CTA whose split range holds stage x of the remainder.
+__device__ __forceinline__ int sk_owner(const MainParams& p, int64_t x) {
+  const int64_t len = static_cast<int64_t>(p.sk_tiles) * (p.num_kt + p.num_lt);
+  return static_cast<int>(((x + 1) * p.sk_ctas - 1) / len);
+}
+
+// Partial-tile slot of CTA c's piece of split tile j: 0 for the first tile of
+// its range, 1 for the last (a range holds at most two pieces that are not
+// whole tiles).
+template <int BN>
+__device__ __forceinline__ float* sk_slot(const MainParams& p, int c, int j) {
+  const int total = p.num_kt + p.num_lt;
+  const int64_t len = static_cast<int64_t>(p.sk_tiles) * total;
+  const int first = static_cast<int>((len * c / p.sk_ctas) / total);
+  return p.partials + static_cast<int64_t>(2 * c + (j == first ? 0 : 1)) * (kTileP * BN);
+}
+
+// Walks this CTA's stages one at a time (or n at a time) across its pieces.
+struct StageCursor {
+  int idx, tile, sb, se, s;
+  bool valid;
+  __device__ __forceinline__ void init(const MainParams& p, int cta, int grid) {
+    idx = 0;
+    valid = main_piece(p, cta, grid, 0, tile, sb, se);
+    s = sb;
+  }
+  __device__ __forceinline__ void advance(const MainParams& p, int cta, int grid, int n) {
+    s += n;
+    while (valid && s >= se) {
+      const int carry = s - se;
+      ++idx;
+      valid = main_piece(p, cta, grid, idx, tile, sb, se);
+      s = sb + carry;
+    }
+  }
+};
+
+// Partial tiles go through L2 only (another SM reads them).
+__device__ __forceinline__ void st_global_cg_f32(float* ptr, float v) {
+  asm volatile("st.global.cg.f32 [%0], %1;" ::"l"(ptr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_global_cg_f32(const float* ptr) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+// Persistent, one CTA per SM.  Two TMEM accumulators let the epilogue of one
+// piece overlap the main loop of the next.  NF4 codes (and, when kAbsTma, the
+// absmax values) of each stage arrive by TMA in a ring of their own; TMA
+// zero-fills rows and columns outside W, so outside W the dequantised operand
+// is zero without per-thread bounds checks.
 template <int BN, bool kTrans, bool kAbsTma>
 __global__ void __launch_bounds__(kMainThreads, 1)
     lora_main_kernel(const __grid_constant__ CUtensorMap map_act,    // X or dY, box {64, BN}
@@ -415,39 +526,45 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                      const __grid_constant__ CUtensorMap map_abs,    // absmax [N, K/64]; Y box {4, 128}, dX box {4, 64}
                      const MainParams p) {
   using S = MainSmem<BN>;
+  constexpr int kMainStages = S::kStages;
+  constexpr int kRaw = S::kRaw;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_abort;
   __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_last;
 
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   const uint32_t bar0 = base + S::kBarOffset;
-  auto full_act = [&](int i) { return bar0 + 8u * i; };
-  auto full_w = [&](int i) { return bar0 + 8u * (kMainStages + i); };
-  auto empty = [&](int i) { return bar0 + 8u * (2 * kMainStages + i); };
-  auto raw_full = [&](int i) { return bar0 + 8u * (3 * kMainStages + i); };
-  auto raw_empty = [&](int i) { return bar0 + 8u * (3 * kMainStages + kRawStages + i); };
-  auto tmem_full = [&](int a) { return bar0 + 8u * (3 * kMainStages + 2 * kRawStages + a); };
-  auto tmem_empty = [&](int a) { return bar0 + 8u * (3 * kMainStages + 2 * kRawStages + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (3 * kMainStages + 2 * kRawStages + 4);
+  // full(i): the stage's token tile (TMA bytes, one producer arrival) and its W
+  // tile (one arrival per dequant warp of the group) are both in place
+  auto full = [&](int i) { return bar0 + 8u * i; };
+  auto empty = [&](int i) { return bar0 + 8u * (kMainStages + i); };
+  auto raw_full = [&](int i) { return bar0 + 8u * (2 * kMainStages + i); };
+  auto raw_empty = [&](int i) { return bar0 + 8u * (2 * kMainStages + kRaw + i); };
+  auto tmem_full = [&](int a) { return bar0 + 8u * (2 * kMainStages + 2 * kRaw + a); };
+  auto tmem_empty = [&](int a) { return bar0 + 8u * (2 * kMainStages + 2 * kRaw + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kMainStages + 2 * kRaw + 4);
   auto raw_slot = [&](int i) { return base + S::kRawOffset + static_cast<uint32_t>(i * S::kRawBytes); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = p.num_kt + p.num_lt;
-  const int num_tiles = p.p_tiles * p.t_tiles;
+  const int cta = static_cast<int>(blockIdx.x);
   const int grid = static_cast<int>(gridDim.x);
-  const int tiles_here = (num_tiles - static_cast<int>(blockIdx.x) + grid - 1) / grid;
-  const int g_end = tiles_here * total;   // stages this CTA runs
+  int g_end = 0;   // stages this CTA runs
+  {
+    int tile, sb, se;
+    for (int idx = 0; main_piece(p, cta, grid, idx, tile, sb, se); ++idx) g_end += se - sb;
+  }
   Abort ab{&s_abort, p.status};
 
   if (threadIdx.x == 0) {
     s_abort = 0;
     for (int i = 0; i < kMainStages; ++i) {
-      mbar_init(full_act(i), 1);    // TMA transaction bytes
-      mbar_init(full_w(i), 4);      // the 4 warps of one dequant group
+      mbar_init(full(i), 5);        // producer (with TMA bytes) + the 4 warps of one dequant group
       mbar_init(empty(i), 1);       // MMA commit
     }
-    for (int i = 0; i < kRawStages; ++i) {
+    for (int i = 0; i < kRaw; ++i) {
       mbar_init(raw_full(i), 1);    // TMA transaction bytes (or a plain arrive for LoRA stages)
       mbar_init(raw_empty(i), 4);   // the 4 warps of the group that reads the slot
     }
@@ -476,81 +593,81 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     // ---------------- TMA producer for the token operand (and the LoRA stages)
     if (lane == 0) {
       int g = 0;
-      int s = 0, p0 = static_cast<int>(blockIdx.x % p.p_tiles) * kTileP;
-      int t0 = static_cast<int>(blockIdx.x / p.p_tiles) * BN;
-      int tile = blockIdx.x;
-      bool lora_ready = false;
-      for (; g < g_end; ++g) {
-        const int slot = g & (kMainStages - 1);
-        if (!mbar_wait(empty(slot), ((g / kMainStages) & 1) ^ 1, ab)) break;
-        const uint32_t act = base + slot * S::kStageBytes;
-        if (s < p.num_kt) {
-          mbar_arrive_expect_tx(full_act(slot), S::kActBytes);
-          tma_load_2d(act, &map_act, full_act(slot), s * kTileK, t0);
-        } else {
-          if (!lora_ready) {
-            // the low-rank activations come from the previous kernel: wait for it
-            // here (the NF4 stages before this point only read the call's inputs),
-            // then let the next kernel start on SMs this grid frees.
-            griddep_wait();
-            griddep_launch_dependents();
-            lora_ready = true;
+      bool lora_ready = false, stop = false;
+      int tile, sb, se;
+      for (int idx = 0; !stop && main_piece(p, cta, grid, idx, tile, sb, se); ++idx) {
+        const int p0 = (tile % p.p_tiles) * kTileP;
+        const int t0 = (tile / p.p_tiles) * BN;
+        for (int s = sb; s < se; ++s, ++g) {
+          const int slot = g & (kMainStages - 1);
+          if (!mbar_wait(empty(slot), ((g / kMainStages) & 1) ^ 1, ab)) {
+            stop = true;
+            break;
           }
-          const int j = s - p.num_kt;
-          mbar_arrive_expect_tx(full_act(slot), S::kActBytes + S::kWBytes);
-          tma_load_2d(act, &map_lact, full_act(slot), j * kTileK, t0);
-          if (kTrans) {
-            // A [K, r] rows p0..p0+127, LoRA columns 64j..: K-major
-            tma_load_2d(act + S::kActBytes, &map_lw, full_act(slot), j * kTileK, p0);
+          const uint32_t act = base + slot * S::kStageBytes;
+          if (s < p.num_kt) {
+            mbar_arrive_expect_tx(full(slot), S::kActBytes);
+            tma_load_2d(act, &map_act, full(slot), s * kTileK, t0);
           } else {
-            // B [r, N] rows 64j.. (the LoRA contraction), columns p0..p0+127: MN-major
-            tma_load_2d(act + S::kActBytes, &map_lw, full_act(slot), p0, j * kTileK);
-            tma_load_2d(act + S::kActBytes + 8192, &map_lw, full_act(slot), p0 + 64, j * kTileK);
+            if (!lora_ready) {
+              // the low-rank activations come from the previous kernel: wait for it
+              // here (the NF4 stages before this point only read the call's inputs),
+              // then let the next kernel start on SMs this grid frees.
+              griddep_wait();
+              griddep_launch_dependents();
+              lora_ready = true;
+            }
+            const int j = s - p.num_kt;
+            mbar_arrive_expect_tx(full(slot), S::kActBytes + S::kWBytes);
+            tma_load_2d(act, &map_lact, full(slot), j * kTileK, t0);
+            if (kTrans) {
+              // A [K, r] rows p0..p0+127, LoRA columns 64j..: K-major
+              tma_load_2d(act + S::kActBytes, &map_lw, full(slot), j * kTileK, p0);
+            } else {
+              // B [r, N] rows 64j.. (the LoRA contraction), columns p0..p0+127: MN-major
+              tma_load_2d(act + S::kActBytes, &map_lw, full(slot), p0, j * kTileK);
+              tma_load_2d(act + S::kActBytes + 8192, &map_lw, full(slot), p0 + 64, j * kTileK);
+            }
           }
-        }
-        if (++s == total) {
-          s = 0;
-          tile += grid;
-          p0 = (tile % p.p_tiles) * kTileP;
-          t0 = (tile / p.p_tiles) * BN;
         }
       }
       // wait (bounded) until every issued load has landed
       for (int q = g - 1; q >= 0 && q >= g - kMainStages; --q)
-        mbar_wait(full_act(q % kMainStages), (q / kMainStages) & 1, ab, false);
+        mbar_wait(full(q % kMainStages), (q / kMainStages) & 1, ab, false);
     }
     __syncwarp();
   } else if (warp == 14) {
     // ---------------- TMA producer for the NF4 codes and absmax
     if (lane == 0) {
       int g = 0;
-      int s = 0, p0 = static_cast<int>(blockIdx.x % p.p_tiles) * kTileP;
-      int tile = blockIdx.x;
-      for (; g < g_end; ++g) {
-        const int slot = g & (kRawStages - 1);
-        if (!mbar_wait(raw_empty(slot), ((g / kRawStages) & 1) ^ 1, ab)) break;
-        if (s >= p.num_kt) {
-          mbar_arrive(raw_full(slot));   // LoRA stage: nothing to load, keep the phases in step
-        } else {
-          const uint32_t dst = raw_slot(slot);
-          mbar_arrive_expect_tx(raw_full(slot), kAbsTma ? (kTrans ? S::kCodeBytes + 1024 : S::kRawBytes)
-                                                        : S::kCodeBytes);
-          if (!kTrans) {
-            tma_load_2d(dst, &map_code, raw_full(slot), 32 * s, p0);                  // W[p0.., 64s..]
-            if (kAbsTma) tma_load_2d(dst + S::kCodeBytes, &map_abs, raw_full(slot), s & ~3, p0);
+      bool stop = false;
+      int tile, sb, se;
+      for (int idx = 0; !stop && main_piece(p, cta, grid, idx, tile, sb, se); ++idx) {
+        const int p0 = (tile % p.p_tiles) * kTileP;
+        for (int s = sb; s < se; ++s, ++g) {
+          const int slot = g & (kRaw - 1);
+          if (!mbar_wait(raw_empty(slot), ((g / kRaw) & 1) ^ 1, ab)) {
+            stop = true;
+            break;
+          }
+          if (s >= p.num_kt) {
+            mbar_arrive(raw_full(slot));   // LoRA stage: nothing to load, keep the phases in step
           } else {
-            tma_load_2d(dst, &map_code, raw_full(slot), p0 >> 1, 64 * s);             // W[64s.., p0..]
-            if (kAbsTma) tma_load_2d(dst + S::kCodeBytes, &map_abs, raw_full(slot), (p0 >> 6) & ~3, 64 * s);
+            const uint32_t dst = raw_slot(slot);
+            mbar_arrive_expect_tx(raw_full(slot), kAbsTma ? (kTrans ? S::kCodeBytes + 1024 : S::kRawBytes)
+                                                          : S::kCodeBytes);
+            if (!kTrans) {
+              tma_load_2d(dst, &map_code, raw_full(slot), 32 * s, p0);                  // W[p0.., 64s..]
+              if (kAbsTma) tma_load_2d(dst + S::kCodeBytes, &map_abs, raw_full(slot), s & ~3, p0);
+            } else {
+              tma_load_2d(dst, &map_code, raw_full(slot), p0 >> 1, 64 * s);             // W[64s.., p0..]
+              if (kAbsTma) tma_load_2d(dst + S::kCodeBytes, &map_abs, raw_full(slot), (p0 >> 6) & ~3, 64 * s);
+            }
           }
         }
-        if (++s == total) {
-          s = 0;
-          tile += grid;
-          p0 = (tile % p.p_tiles) * kTileP;
-        }
       }
-      for (int q = g - 1; q >= 0 && q >= g - kRawStages; --q)
-        mbar_wait(raw_full(q % kRawStages), (q / kRawStages) & 1, ab, false);
+      for (int q = g - 1; q >= 0 && q >= g - kRaw; --q)
+        mbar_wait(raw_full(q % kRaw), (q / kRaw) & 1, ab, false);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -559,33 +676,48 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       // A operand majorness: Y -- W tile K-major, B tile MN-major; dX -- W tile MN-major, A tile K-major
       constexpr uint32_t idesc_w = umma_idesc_bf16(kTileP, BN, kTrans ? 1 : 0, 0);
       constexpr uint32_t idesc_l = umma_idesc_bf16(kTileP, BN, kTrans ? 0 : 1, 0);
+      // descriptors: fixed fields once, the start address (16-byte units) added per MMA
+      const uint64_t a_hi_k = sw128_desc(0, 16, 1024), a_hi_mn = sw128_desc(0, 8192, 1024);
+      const uint64_t b_hi = sw128_desc(0, 16, 1024);
+      const uint32_t base16 = (base & 0x3FFFFu) >> 4;
+      // the four K=16 steps of one stage: D (+)= W tile . token tile^T
+      auto issue_stage = [&](uint32_t tmem_d, int slot, bool lora, bool first) {
+        const bool a_mn = (kTrans != lora);
+        const uint64_t a_hi = a_mn ? a_hi_mn : a_hi_k;
+        const uint32_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);
+        const uint32_t idesc = lora ? idesc_l : idesc_w;
+        const uint32_t b0 = base16 + static_cast<uint32_t>(slot) * (S::kStageBytes >> 4);
+        const uint32_t a0 = b0 + (S::kActBytes >> 4);
+        umma_bf16(tmem_d, a_hi | a0, b_hi | b0, idesc, first ? 0u : 1u);
+        umma_bf16(tmem_d, a_hi | (a0 + a_step), b_hi | (b0 + 2u), idesc, 1u);
+        umma_bf16(tmem_d, a_hi | (a0 + 2u * a_step), b_hi | (b0 + 4u), idesc, 1u);
+        umma_bf16(tmem_d, a_hi | (a0 + 3u * a_step), b_hi | (b0 + 6u), idesc, 1u);
+      };
       int g = 0;
-      int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += grid, ++it) {
-        const int acc = it & 1;
+      int tile, sb, se;
+      for (int idx = 0; ok && main_piece(p, cta, grid, idx, tile, sb, se); ++idx) {
+        const int acc = idx & 1;
         const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(acc * BN);
-        if (!mbar_wait(tmem_empty(acc), ((it >> 1) & 1) ^ 1, ab)) break;
+        if (!mbar_wait(tmem_empty(acc), ((idx >> 1) & 1) ^ 1, ab)) break;
         tc_fence_after_sync();
-        for (int s = 0; s < total; ++s, ++g) {
-          const int slot = g % kMainStages;
-          const uint32_t ph = (g / kMainStages) & 1;
-          if (!mbar_wait(full_act(slot), ph, ab) || !mbar_wait(full_w(slot), ph, ab)) {
+        int s = sb;
+        while (s < se) {
+          const int slot = g & (kMainStages - 1);
+          if (!mbar_wait(full(slot), (g / kMainStages) & 1, ab)) {
             ok = false;
             break;
           }
+          // when the next stage of the piece is in place too, issue both at once
+          const int slot2 = (g + 1) & (kMainStages - 1);
+          const bool two = (s + 1 < se) && mbar_test_wait(full(slot2), ((g + 1) / kMainStages) & 1);
           tc_fence_after_sync();
-          const uint32_t act = base + slot * S::kStageBytes;
-          const uint32_t wt = act + S::kActBytes;
-          const bool lora = s >= p.num_kt;
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const bool a_mn = (kTrans != lora);
-            const uint64_t ad = a_mn ? sw128_desc(wt + kk * 2048, 8192, 1024) : sw128_desc(wt + kk * 32, 16, 1024);
-            const uint64_t bd = sw128_desc(act + kk * 32, 16, 1024);
-            umma_bf16(tmem_d, ad, bd, lora ? idesc_l : idesc_w, (s | kk) != 0 ? 1u : 0u);
-          }
+          issue_stage(tmem_d, slot, s >= p.num_kt, s == sb);
+          if (two) issue_stage(tmem_d, slot2, s + 1 >= p.num_kt, false);
           umma_commit(empty(slot));
+          if (two) umma_commit(empty(slot2));
+          s += two ? 2 : 1;
+          g += two ? 2 : 1;
         }
         if (ok) umma_commit(tmem_full(acc));
       }
@@ -631,32 +763,28 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (n >= p.N || kb >= kblocks) return 0.0f;
       return ldg_nc_f32(p.absmax + static_cast<int64_t>(n) * kblocks + kb);
     };
-    // stage g = tile_it * total + s; this group takes every other g
-    int s = grp, tile = blockIdx.x;
-    int p0 = (tile % p.p_tiles) * kTileP;
-    auto advance = [&](int& ss, int& tt, int& pp) {
-      ss += 2;
-      while (ss >= total) {
-        ss -= total;
-        tt += grid;
-        pp = (tt % p.p_tiles) * kTileP;
-      }
-    };
-    int s_next = s, tile_next = tile, p0_next = p0;
-    advance(s_next, tile_next, p0_next);
-    float am_next = (grp < g_end) ? absmax_direct(s, p0) : 0.0f;
+    // this group takes every other stage of the CTA's stage sequence
+    StageCursor cur, nxt;
+    cur.init(p, cta, grid);
+    cur.advance(p, cta, grid, grp);
+    nxt = cur;
+    nxt.advance(p, cta, grid, 2);
+    float am_next = (grp < g_end) ? absmax_direct(cur.s, (cur.tile % p.p_tiles) * kTileP) : 0.0f;
     for (int g = grp; g < g_end; g += 2) {
+      const int s = cur.s;
+      const int p0 = (cur.tile % p.p_tiles) * kTileP;
       const float am_direct = am_next;
-      am_next = (g + 2 < g_end) ? absmax_direct(s_next, p0_next) : 0.0f;
+      am_next = (g + 2 < g_end) ? absmax_direct(nxt.s, (nxt.tile % p.p_tiles) * kTileP) : 0.0f;
       const int slot = g & (kMainStages - 1);
       const uint32_t ph = (g / kMainStages) & 1;
+      const int rslot = g & (kRaw - 1);
       // every lane acquires the TMA-written codes itself (a shuffle does not order memory)
-      if (!__all_sync(0xffffffffu, mbar_wait(raw_full(slot), ph, ab))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(raw_full(rslot), (g / kRaw) & 1, ab))) break;
       uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
       float am = am_direct;
       const bool nf4 = s < p.num_kt;
       if (nf4) {
-        const uint32_t rs = raw_slot(slot);
+        const uint32_t rs = raw_slot(rslot);
         c0 = ld_shared_v4(rs + code_off[0]);
         c1 = ld_shared_v4(rs + code_off[1]);
         if (kAbsTma) {
@@ -675,15 +803,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         fence_proxy_async_smem();
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(full_w(slot));
+      if (lane == 0) mbar_arrive(full(slot));
       // release the code slot only now: the codes have been consumed, so the loads
       // that read them have completed.  Released right after issuing the loads, the
       // TMA refill of the slot could land before a lane's load had read it.
-      if (lane == 0) mbar_arrive(raw_empty(slot));
-      s = s_next;
-      tile = tile_next;
-      p0 = p0_next;
-      advance(s_next, tile_next, p0_next);
+      if (lane == 0) mbar_arrive(raw_empty(rslot));
+      cur = nxt;
+      nxt.advance(p, cta, grid, 2);
     }
   } else if (warp >= 10 && warp < 14) {
     // ---------------- epilogue: TMEM -> bf16 -> staging -> TMA store
@@ -698,44 +824,98 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const uint32_t chunk16 = static_cast<uint32_t>((f_even & 63) >> 3);
     const uint32_t in16 = static_cast<uint32_t>((f_even & 7) * 2);
     const bool odd = (lane & 1) != 0;
-    int it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += grid, ++it) {
+    // one chunk of 32 tokens x 128 features (this thread: feature prow) -> bf16 -> Y / dX
+    auto store_chunk = [&](const float (&f)[32], int p0, int t0, int c0) {
+      // the previous chunk's store must have read the staging buffer
+      if (leader) tma_store_wait_read_all();
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int jj = 0; jj < kEpiChunk / 2; ++jj) {
+        // tokens a and a + 4: their swizzled rows use disjoint bank groups.
+        // even lane: token a, features (f, f+1); odd lane: token a+4, features (f-1, f)
+        const int a = (jj & 3) + (jj >> 2) * 8;
+        const float mine = odd ? f[a + 4] : f[a];
+        const float give = odd ? f[a] : f[a + 4];
+        const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+        const uint32_t pair = odd ? pack_bf16x2(got, mine) : pack_bf16x2(mine, got);
+        const uint32_t tok = static_cast<uint32_t>(a + (odd ? 4 : 0));
+        st_shared_u32(staging + half_off + tok * 128u + ((chunk16 ^ (tok & 7u)) << 4) + in16, pair);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 128);
+      if (leader && t0 + c0 < p.M) {   // boxes wholly past the last token / feature are not stored
+        tma_store_2d(&map_out, staging, p0, t0 + c0);
+        if (p0 + 64 < (kTrans ? p.K : p.N)) tma_store_2d(&map_out, staging + 4096, p0 + 64, t0 + c0);
+        tma_store_commit();
+      }
+    };
+    int tile, sb, se;
+    for (int idx = 0; main_piece(p, cta, grid, idx, tile, sb, se); ++idx) {
       const int p0 = (tile % p.p_tiles) * kTileP;
       const int t0 = (tile / p.p_tiles) * BN;
-      const int acc = it & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(tmem_full(acc), (it >> 1) & 1, ab))) break;
+      const int acc = idx & 1;
+      const uint32_t tacc = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
+      if (!__all_sync(0xffffffffu, mbar_wait(tmem_full(acc), (idx >> 1) & 1, ab))) break;
       tc_fence_after_sync();
+      if (sb == 0 && se == total) {
+        // a whole tile: straight to the output
+        for (int c0 = 0; c0 < BN; c0 += kEpiChunk) {
+          uint32_t v[32];
+          tmem_ld32(tacc + c0, v);
+          tmem_ld_wait();
+          float f[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) f[q] = __uint_as_float(v[q]);
+          store_chunk(f, p0, t0, c0);
+        }
+        // this accumulator may be overwritten by the MMA of piece idx + 2
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tmem_empty(acc));
+        continue;
+      }
+      // a piece of a split tile: fp32 partial to this CTA's slot, token-major
+      // ([token][feature]) so that each warp store covers 128 contiguous bytes
+      const int j = tile - p.dp_tiles;
+      float* col = sk_slot<BN>(p, cta, j) + prow;
       for (int c0 = 0; c0 < BN; c0 += kEpiChunk) {
         uint32_t v[32];
-        tmem_ld32(tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16) + c0, v);
+        tmem_ld32(tacc + c0, v);
         tmem_ld_wait();
-        // the previous chunk's store must have read the staging buffer
-        if (leader) tma_store_wait_read_all();
-        named_bar_sync(1, 128);
 #pragma unroll
-        for (int jj = 0; jj < kEpiChunk / 2; ++jj) {
-          // tokens a and a + 4: their swizzled rows use disjoint bank groups.
-          // even lane: token a, features (f, f+1); odd lane: token a+4, features (f-1, f)
-          const int a = (jj & 3) + (jj >> 2) * 8;
-          const float mine = __uint_as_float(odd ? v[a + 4] : v[a]);
-          const float give = __uint_as_float(odd ? v[a] : v[a + 4]);
-          const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-          const uint32_t pair = odd ? pack_bf16x2(got, mine) : pack_bf16x2(mine, got);
-          const uint32_t tok = static_cast<uint32_t>(a + (odd ? 4 : 0));
-          st_shared_u32(staging + half_off + tok * 128u + ((chunk16 ^ (tok & 7u)) << 4) + in16, pair);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (leader && t0 + c0 < p.M) {   // boxes wholly past the last token / feature are not stored
-          tma_store_2d(&map_out, staging, p0, t0 + c0);
-          if (p0 + 64 < (kTrans ? p.K : p.N)) tma_store_2d(&map_out, staging + 4096, p0 + 64, t0 + c0);
-          tma_store_commit();
-        }
+        for (int q = 0; q < 32; ++q) st_global_cg_f32(col + (c0 + q) * kTileP, __uint_as_float(v[q]));
       }
-      // this accumulator may be overwritten by the MMA of tile it + 2
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(tmem_empty(acc));
+      // publish the partial; the last piece of the tile to get here finishes it
+      __threadfence();
+      named_bar_sync(1, 128);
+      const int64_t tile_first = static_cast<int64_t>(j) * total;
+      const int c_first = sk_owner(p, tile_first);
+      const int c_last = sk_owner(p, tile_first + total - 1);
+      if (leader) {
+        // the counters were zeroed by the previous kernel
+        griddep_wait();
+        const int before = atomicAdd(p.counters + j, 1);
+        s_last = (before == c_last - c_first) ? 1 : 0;
+      }
+      named_bar_sync(1, 128);
+      if (!s_last) continue;
+      __threadfence();
+      // contraction order: the CTA holding the first stages comes first
+      const float* src_first = sk_slot<BN>(p, c_first, j) + prow;
+      for (int c0 = 0; c0 < BN; c0 += kEpiChunk) {
+        float f[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) f[q] = ld_global_cg_f32(src_first + (c0 + q) * kTileP);
+        for (int c = c_first + 1; c <= c_last; ++c) {
+          const float* src = sk_slot<BN>(p, c, j) + prow;
+#pragma unroll
+          for (int q = 0; q < 32; ++q) f[q] += ld_global_cg_f32(src + (c0 + q) * kTileP);
+        }
+        store_chunk(f, p0, t0, c0);
+      }
     }
     if (leader) tma_store_wait_all();
   }
@@ -868,17 +1048,56 @@ cudaError_t launch_skinny(int rp, const CUtensorMap (&maps)[4], const SkinnyPara
   return launch_skinny_split<MODE, 128>(maps, sp, tiles, split, pdl, stream);
 }
 
+// Split-remainder buffers the main kernel may use (from the workspace).
+struct SplitBuffers {
+  float* partials;
+  size_t partial_bytes;
+  int* counters;
+  int counter_cap;
+};
+
+// Whole tiles for the full waves, then the stages of the remaining tiles
+// shared evenly by the CTAs (at least kMinSkStages each), when the buffers
+// for the partial tiles are there; otherwise whole tiles only.
+int plan_schedule(int tiles, int total, int bn, const SplitBuffers& sb, MainParams& mp) {
+  const int sms = sm_count();
+  const int full = tiles / sms, rem = tiles % sms;
+  mp.sk_tiles = 0;
+  mp.sk_ctas = 0;
+  if (rem != 0 && sb.partials != nullptr && sb.counters != nullptr) {
+    const int64_t len = static_cast<int64_t>(rem) * total;
+    // never fewer CTAs than remaining tiles (that would be worse than whole tiles)
+    const int ctas = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(rem, len / kMinSkStages)));
+    const size_t need = static_cast<size_t>(2) * ctas * kTileP * bn * sizeof(float);
+    if (need <= sb.partial_bytes && rem <= sb.counter_cap) {
+      mp.dp_tiles = full * sms;
+      mp.dp_rounds = full;
+      mp.sk_tiles = rem;
+      mp.sk_ctas = ctas;
+      mp.partials = sb.partials;
+      mp.counters = sb.counters;
+      return full > 0 ? sms : ctas;
+    }
+  }
+  const int grid = std::min(tiles, sms);
+  mp.dp_tiles = tiles;
+  mp.dp_rounds = (tiles + grid - 1) / grid;
+  mp.partials = nullptr;
+  mp.counters = nullptr;
+  return grid;
+}
+
 template <int BN, bool kTrans, bool kAbsTma>
-cudaError_t launch_main_bn(const CUtensorMap (&maps)[6], MainParams mp, int P, int M,
+cudaError_t launch_main_bn(const CUtensorMap (&maps)[6], MainParams mp, int P, int M, const SplitBuffers& sb,
                            cudaStream_t stream) {
   auto kern = lora_main_kernel<BN, kTrans, kAbsTma>;
   cudaError_t e = set_smem(kern, MainSmem<BN>::kBytes);
   if (e != cudaSuccess) return e;
   mp.p_tiles = (P + kTileP - 1) / kTileP;
   mp.t_tiles = (M + BN - 1) / BN;
-  const int tiles = mp.p_tiles * mp.t_tiles;
+  const int grid = plan_schedule(mp.p_tiles * mp.t_tiles, mp.num_kt + mp.num_lt, BN, sb, mp);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(std::min(tiles, sm_count()), 1, 1);
+  cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kMainThreads, 1, 1);
   cfg.dynamicSmemBytes = MainSmem<BN>::kBytes;
   cfg.stream = stream;
@@ -895,12 +1114,12 @@ cudaError_t launch_main_bn(const CUtensorMap (&maps)[6], MainParams mp, int P, i
 
 template <int BN, bool kTrans>
 cudaError_t launch_main_abs(const CUtensorMap (&maps)[6], const MainParams& mp, bool abs_tma, int P,
-                            int M, cudaStream_t stream) {
-  if (abs_tma) return launch_main_bn<BN, kTrans, true>(maps, mp, P, M, stream);
-  return launch_main_bn<BN, kTrans, false>(maps, mp, P, M, stream);
+                            int M, const SplitBuffers& sb, cudaStream_t stream) {
+  if (abs_tma) return launch_main_bn<BN, kTrans, true>(maps, mp, P, M, sb, stream);
+  return launch_main_bn<BN, kTrans, false>(maps, mp, P, M, sb, stream);
 }
 
-int pick_bn(int M) { return M <= 64 ? 64 : (M <= 128 ? 128 : 256); }
+int pick_bn(int M) { return M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256)); }
 
 // The low-rank weight the kernels read: A itself when its rows are 16-byte
 // multiples (r % 8 == 0), else the zero-padded copy [K, rp] in the workspace.
@@ -920,7 +1139,7 @@ LowRankA low_rank_a(const LayerDims& d, const uint16_t* A, const Workspace& ws) 
 template <bool kTrans>
 cudaError_t launch_main(const LayerDims& d, const uint16_t* act, const uint16_t* lact,
                         const uint16_t* lw, int lw_cols, uint16_t* out, const uint8_t* packed,
-                        const float* absmax, int* status, cudaStream_t stream) {
+                        const float* absmax, const Workspace& ws, int* status, cudaStream_t stream) {
   const int P = kTrans ? d.K : d.N;     // output features
   const int C = kTrans ? d.N : d.K;     // contraction length of the NF4 part
   const int bn = pick_bn(d.M);
@@ -949,9 +1168,11 @@ cudaError_t launch_main(const LayerDims& d, const uint16_t* act, const uint16_t*
   mp.num_kt = (C + kTileK - 1) / kTileK;
   mp.num_lt = d.rp / kTileK;
   mp.status = status;
-  if (bn == 64) return launch_main_abs<64, kTrans>(maps, mp, abs_tma, P, d.M, stream);
-  if (bn == 128) return launch_main_abs<128, kTrans>(maps, mp, abs_tma, P, d.M, stream);
-  return launch_main_abs<256, kTrans>(maps, mp, abs_tma, P, d.M, stream);
+  const SplitBuffers sb = {ws.partials, ws.partial_bytes, ws.counters, ws.counter_cap};
+  if (bn == 32) return launch_main_abs<32, kTrans>(maps, mp, abs_tma, P, d.M, sb, stream);
+  if (bn == 64) return launch_main_abs<64, kTrans>(maps, mp, abs_tma, P, d.M, sb, stream);
+  if (bn == 128) return launch_main_abs<128, kTrans>(maps, mp, abs_tma, P, d.M, sb, stream);
+  return launch_main_abs<256, kTrans>(maps, mp, abs_tma, P, d.M, sb, stream);
 }
 
 // Pads A to [K, rp] (only needed when r % 8 != 0).
@@ -977,9 +1198,16 @@ size_t align_up(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 
 }  // namespace
 
+// Workspace: padded A [K, rp], bf16(s*T) and bf16(s*G) [M, rp], then the main
+// kernel's split-tile counters (one per SM) and partial tiles (two per SM).
+size_t split_partial_bytes(const LayerDims& d) {
+  return static_cast<size_t>(2) * sm_count() * kTileP * pick_bn(d.M) * sizeof(float);
+}
+
 size_t workspace_bytes(const LayerDims& d) {
   const size_t rp = static_cast<size_t>(d.rp);
-  return align_up(static_cast<size_t>(d.K) * rp * 2) + 2 * align_up(static_cast<size_t>(d.M) * rp * 2);
+  return align_up(static_cast<size_t>(d.K) * rp * 2) + 2 * align_up(static_cast<size_t>(d.M) * rp * 2) +
+         align_up(static_cast<size_t>(sm_count()) * sizeof(int)) + align_up(split_partial_bytes(d));
 }
 
 Workspace carve_workspace(const LayerDims& d, void* base) {
@@ -991,6 +1219,12 @@ Workspace carve_workspace(const LayerDims& d, void* base) {
   w.s_t = reinterpret_cast<uint16_t*>(b);
   b += align_up(static_cast<size_t>(d.M) * rp * 2);
   w.s_g = reinterpret_cast<uint16_t*>(b);
+  b += align_up(static_cast<size_t>(d.M) * rp * 2);
+  w.counters = reinterpret_cast<int*>(b);
+  w.counter_cap = sm_count();
+  b += align_up(static_cast<size_t>(sm_count()) * sizeof(int));
+  w.partials = reinterpret_cast<float*>(b);
+  w.partial_bytes = split_partial_bytes(d);
   return w;
 }
 
@@ -1016,12 +1250,14 @@ cudaError_t run_forward(const LayerDims& d, const uint16_t* X, const uint8_t* pa
     sp.job[0].tiles = (d.M + kTileP - 1) / kTileP;
     sp.job[0].out_f32 = XA;
     sp.job[0].out_bf16 = ws.s_t;
+    sp.zero = ws.counters;
+    sp.n_zero = ws.counters != nullptr ? ws.counter_cap : 0;
     sp.status = status;
     const int tiles = sp.job[0].tiles;
     e = launch_skinny<kRowsT>(d.rp, maps, sp, tiles, pick_split(tiles, sp.num_ct), stream);
     if (e != cudaSuccess) return e;
   }
-  return launch_main<false>(d, X, ws.s_t, B, d.r, Y, packed, absmax, status, stream);
+  return launch_main<false>(d, X, ws.s_t, B, d.r, Y, packed, absmax, ws, status, stream);
 }
 
 cudaError_t run_backward(const LayerDims& d, const uint16_t* X, const uint16_t* dY,
@@ -1048,6 +1284,8 @@ cudaError_t run_backward(const LayerDims& d, const uint16_t* X, const uint16_t* 
     sp.job[0].out_bf16 = ws.s_g;
     sp.xa = XA;
     sp.s_t = ws.s_t;
+    sp.zero = ws.counters;
+    sp.n_zero = ws.counters != nullptr ? ws.counter_cap : 0;
     sp.status = status;
     const int tiles = sp.job[0].tiles;
     e = launch_skinny<kRowsG>(d.rp, maps, sp, tiles, pick_split(tiles, sp.num_ct), stream);
@@ -1057,7 +1295,7 @@ cudaError_t run_backward(const LayerDims& d, const uint16_t* X, const uint16_t* 
   // before dX finishes because dX lets it go only after its own wait on the G kernel.
   const bool with_dx = dX != nullptr;
   if (with_dx) {
-    e = launch_main<true>(d, dY, ws.s_g, la.ptr, la.cols, dX, packed, absmax, status, stream);
+    e = launch_main<true>(d, dY, ws.s_g, la.ptr, la.cols, dX, packed, absmax, ws, status, stream);
     if (e != cudaSuccess) return e;
   }
   // dA = X^T . bf16(s*G)  -> [K, r]   and   dB = bf16(s*T)^T . dY  -> [r, N], one launch

@@ -101,6 +101,24 @@ extern "C" qlora_status qlora_linear_fwd_noalloc(const uint16_t* X, int64_t M, i
   ws.a_pad = static_cast<uint16_t*>(scratch);
   ws.s_t = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(scratch) + a_pad_bytes);
   ws.s_g = nullptr;   // backward only
+  // what is left of the array holds the split-tile counters and partial tiles
+  // of the main kernel; when they do not fit it takes whole tiles only
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const size_t counter_bytes = round_up_1k(static_cast<size_t>(sms) * sizeof(int));
+  const size_t used = a_pad_bytes + s_t_bytes;
+  ws.counters = nullptr;
+  ws.counter_cap = 0;
+  ws.partials = nullptr;
+  ws.partial_bytes = 0;
+  if (sms > 0 && used + counter_bytes < kNoAllocScratchBytes) {
+    uint8_t* rest = static_cast<uint8_t*>(scratch) + used;
+    ws.counters = reinterpret_cast<int*>(rest);
+    ws.counter_cap = sms;
+    ws.partials = reinterpret_cast<float*>(rest + counter_bytes);
+    ws.partial_bytes = kNoAllocScratchBytes - used - counter_bytes;
+  }
   e = qlora::run_forward(d, X, packed, absmax, A, B, Y, XA_save, ws, status,
                          reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {

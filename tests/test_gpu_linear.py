@@ -86,6 +86,23 @@ def test_token_sweep(m):
     check_layer(synthetic.layer_inputs(sh), sh.s, rows=rows, bwd=(m >= 128))
 
 
+# Shapes whose main-kernel schedule splits tiles across CTAs (few tiles, long
+# contractions), so partial tiles are summed by the last CTA to finish them;
+# the last one also has whole-tile rounds before the split remainder.
+SPLIT = [
+    (16, 4096, 256, 16, 1.0),      # Y: 2 tiles x 65 stages over 8 CTAs
+    (16, 256, 4096, 16, 0.5),      # dX: 2 tiles x 65 stages
+    (40, 4096, 392, 24, 2.0),      # Y: BN 64, ragged feature tile, padded rank
+    (300, 2048, 10240, 16, 1.0),   # Y: 160 tiles = one whole round + 12 split tiles
+]
+
+
+@pytest.mark.parametrize("case", SPLIT, ids=lambda c: "M{}_K{}_N{}_r{}".format(*c[:4]))
+def test_split_tiles_full(case):
+    M, K, N, r, s = case
+    check_layer(_inputs(M, K, N, r, seed=M + N), s)
+
+
 def test_repeat_calls_are_deterministic():
     from tests.parity_utils import run_gpu
     inp = _inputs(384, 512, 256, 16, seed=8)
