@@ -103,6 +103,22 @@ def test_split_tiles_full(case):
     check_layer(_inputs(M, K, N, r, seed=M + N), s)
 
 
+# Schedule edge cases, checked on sampled rows (every output feature of those rows):
+# one tile past a whole number of rounds, split four ways; tiles an exact multiple
+# of the SM count (whole tiles only); dX with the split remainder in the last round.
+EDGE = [
+    (256, 4096, 128 * 149, 16, 1.0),
+    (256, 512, 128 * 148, 8, 2.0),
+    (512, 128 * 150, 1024, 16, 0.5),
+]
+
+
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: "M{}_K{}_N{}_r{}".format(*c[:4]))
+def test_schedule_edges_sampled(case):
+    M, K, N, r, s = case
+    check_layer(_inputs(M, K, N, r, seed=M + 7), s, rows=synthetic.sample_rows(M, n=64))
+
+
 def test_repeat_calls_are_deterministic():
     from tests.parity_utils import run_gpu
     inp = _inputs(384, 512, 256, 16, seed=8)
