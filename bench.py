@@ -414,6 +414,10 @@ def run_ours(args):
                       "share": round(t / sum(v[0] for v in kernels.values()), 4)}
                   for k, (t, n) in sorted(kernels.items(), key=lambda kv: -kv[1][0])}
 
+    # ---- the same steps captured once in a CUDA graph and replayed: launch-amortised
+    # time, reported beside (not instead of) the stream-launched value
+    graph = graph_timing(step, n_sets, flops, world, timed)
+
     # ---- end to end: pinned host buffers, copies inside the timed region
     t0 = sets[0]
     hX = t0["X"].cpu().pin_memory()
@@ -468,6 +472,7 @@ def run_ours(args):
         "profiled_ms_per_step": prof_total_ms / args.steps,
         "gpu_launches": launches,
         "nf4_codec": codec,
+        "cuda_graph": graph,
         "clocks": clocks,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -478,6 +483,31 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def graph_timing(step, n_sets, flops, world, timed, replays=20):
+    """Steps captured in one CUDA graph (a whole number of input-set rotations) and
+    replayed; ms per step over the replays."""
+    import torch
+    per_graph = n_sets * max(1, 16 // n_sets)
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for i in range(per_graph):   # warm the allocator on the capture stream
+                step(i)
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(g):
+            for i in range(per_graph):
+                step(i)
+        g.replay()
+        torch.cuda.synchronize()
+        ms = timed(lambda i: g.replay(), replays) / (replays * per_graph)
+    except Exception as e:   # report, do not fail the run
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
+    return {"ms_per_step": ms, "value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "steps_per_graph": per_graph, "replays": replays}
 
 
 def codec_rooflines(sh, sets, dev, peaks, stream, reps=20):
