@@ -120,6 +120,25 @@ qlora_status qlora_dequant_nf4(const uint8_t* packed, const float* absmax,
                                int64_t n_out, int64_t n_in, uint16_t* W_out,
                                qlora_stream_t stream);
 
+/*
+ * Merged 16-bit weight: the adapter folded into the base weight,
+ *   W_out[n, k] = bf16_rne(fma(s, (A . B)[k, n], W_deq[n, k]))
+ * with W_deq the qlora_dequant_nf4 expansion (bit for bit) and (A . B) the
+ * rank-r product accumulated in fp32 on the tensor core.
+ *   packed, absmax  the NF4 weight [d_out, d_in] as produced by qlora_quantize_nf4 (read);
+ *   A  [d_in, r] bf16 and B [r, d_out] bf16, row-major (read; no alignment needed);
+ *   W_out [d_out, d_in] bf16, written.
+ * Re-quantising the merged weight to NF4 is qlora_quantize_nf4 on W_out.
+ * Requires d_in % 64 == 0, d_out % 8 == 0, 1 <= r <= 128; packed, absmax and
+ * W_out 16-byte aligned.  Asynchronous on `stream`; a device-side wait that
+ * runs out sets the status word (qlora_device_status).
+ * Pages: "这不是“魔法”是把Unsloth的底层优化逻辑榨干了用", section 4
+ * (save_pretrained_merged, "merged_16bit").
+ */
+qlora_status qlora_merge_nf4(const uint8_t* packed, const float* absmax, int64_t d_out, int64_t d_in,
+                             const uint16_t* A, const uint16_t* B, int32_t r, float s, uint16_t* W_out,
+                             qlora_stream_t stream);
+
 /* Bytes of scratch qlora_linear_fwd / qlora_linear_bwd need for this shape
  * (0 if the shape is unsupported).  The same workspace serves both calls. */
 size_t qlora_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int32_t r);

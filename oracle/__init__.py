@@ -2,6 +2,6 @@
 product path never imports it (see ``qlora_oracle`` for what it computes)."""
 from .qlora_oracle import (  # noqa: F401
     BLOCK, NF4_CODE, ZERO_CODE, bf16_bits, bf16_round, code_midpoints,
-    dequantize_nf4, lora_backward, lora_forward, lora_scale, merged_weight,
+    dequantize_nf4, lora_backward, lora_forward, lora_scale, merged_weight, merged_weight_bf16,
     nearest_code, quantize_nf4, unpack_codes,
 )

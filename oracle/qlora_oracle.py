@@ -229,6 +229,14 @@ def merged_weight(W_deq, A, B, s: float) -> np.ndarray:
     return _f64(W_deq) + float(s) * (_f64(A) @ _f64(B)).T
 
 
+def merged_weight_bf16(W_deq, A, B, s: float) -> np.ndarray:
+    """The 16-bit export: merged_weight rounded to bf16 (nearest, ties to even).
+
+    Same page and section as merged_weight (the "merged_16bit" save).
+    """
+    return bf16_round(merged_weight(W_deq, A, B, s))
+
+
 def lora_scale(alpha: float, r: int, rank_stabilised: bool = False) -> float:
     """s = alpha / r, or alpha / sqrt(r) for the rank-stabilised variant."""
     return float(alpha) / (float(np.sqrt(r)) if rank_stabilised else float(r))

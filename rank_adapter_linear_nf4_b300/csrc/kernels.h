@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace qlora {
@@ -18,6 +19,7 @@ enum KernelKind : int {
   kKindRed,
   kKindMainFwd,
   kKindMainDx,
+  kKindMerge,
   kNumKernelKinds
 };
 
@@ -74,6 +76,15 @@ Workspace carve_workspace(const LayerDims& d, void* base);
 cudaError_t run_forward(const LayerDims& d, const uint16_t* X, const uint8_t* packed,
                         const float* absmax, const uint16_t* A, const uint16_t* B, uint16_t* Y,
                         float* XA, const Workspace& ws, int* status, cudaStream_t stream);
+
+// Tensor map over a row-major bf16 [rows, cols] matrix, 128-byte swizzle.
+bool make_bf16_map_sw128(CUtensorMap* m, const void* gaddr, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                         uint32_t box_rows);
+
+// Merged weight bf16(W_deq + s . (A . B)^T) (lora_merge.cu).
+cudaError_t launch_merge_nf4(const uint8_t* packed, const float* absmax, int N, int K, const uint16_t* A,
+                             const uint16_t* B, int r, float s, uint16_t* out, int* status,
+                             cudaStream_t stream);
 
 cudaError_t run_backward(const LayerDims& d, const uint16_t* X, const uint16_t* dY,
                          const uint8_t* packed, const float* absmax, const uint16_t* A,

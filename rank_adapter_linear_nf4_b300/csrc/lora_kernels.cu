@@ -1200,6 +1200,11 @@ size_t align_up(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 
 // Workspace: padded A [K, rp], bf16(s*T) and bf16(s*G) [M, rp], then the main
 // kernel's split-tile counters (one per SM) and partial tiles (two per SM).
+bool make_bf16_map_sw128(CUtensorMap* m, const void* gaddr, uint64_t cols, uint64_t rows, uint32_t box_cols,
+                         uint32_t box_rows) {
+  return map_bf16(m, gaddr, cols, rows, box_cols, box_rows, true);
+}
+
 size_t split_partial_bytes(const LayerDims& d) {
   return static_cast<size_t>(2) * sm_count() * kTileP * pick_bn(d.M) * sizeof(float);
 }

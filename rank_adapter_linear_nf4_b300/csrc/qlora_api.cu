@@ -86,7 +86,7 @@ std::vector<cudaEvent_t> g_free_events;
 
 const char* const kKindNames[qlora::kNumKernelKinds] = {
     "nf4_quantize", "nf4_dequant", "lora_pad_A", "lora_rows_T", "lora_rows_G",
-    "lora_red_dA_dB", "lora_main_fwd", "lora_main_dX"};
+    "lora_red_dA_dB", "lora_main_fwd", "lora_main_dX", "lora_merge"};
 
 cudaEvent_t take_event() {
   if (!g_free_events.empty()) {
@@ -227,6 +227,23 @@ qlora_status qlora_dequant_nf4(const uint8_t* packed, const float* absmax, int64
   if (!aligned16(packed) || !aligned16(absmax) || !aligned16(W_out)) return QLORA_ERR_ALIGN;
   cudaError_t e = qlora::launch_dequant_nf4(packed, absmax, n_out * n_in, W_out,
                                             reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+qlora_status qlora_merge_nf4(const uint8_t* packed, const float* absmax, int64_t d_out, int64_t d_in,
+                             const uint16_t* A, const uint16_t* B, int32_t r, float s, uint16_t* W_out,
+                             qlora_stream_t stream) {
+  if (d_out < 1 || d_in < 1) return QLORA_ERR_SHAPE;
+  const int64_t max_dim = (int64_t(1) << 31) - 1;
+  if (d_out > max_dim || d_in > max_dim || (d_out + 127) / 128 > 65535) return QLORA_ERR_SHAPE;
+  if (d_in % 64 != 0 || d_out % 8 != 0 || r < 1 || r > 128) return QLORA_ERR_UNSUPPORTED;
+  if (!packed || !absmax || !A || !B || !W_out) return QLORA_ERR_NULL;
+  if (!aligned16(packed) || !aligned16(absmax) || !aligned16(W_out)) return QLORA_ERR_ALIGN;
+  int cuda_error = 0;
+  int* status = qlora::device_status_word(&cuda_error);
+  if (status == nullptr) return cuda_fail(static_cast<cudaError_t>(cuda_error));
+  cudaError_t e = qlora::launch_merge_nf4(packed, absmax, static_cast<int>(d_out), static_cast<int>(d_in), A, B, r,
+                                          s, W_out, status, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
 }
 

@@ -42,6 +42,8 @@ _SIGNATURES = {
     "qlora_linear_fwd_noalloc": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p,
                                                 _c_void_p, _c_void_p, _i32, _f32, _c_void_p, _c_void_p,
                                                 _c_void_p]),
+    "qlora_merge_nf4": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p, _i32, _f32,
+                                       _c_void_p, _c_void_p]),
     "qlora_linear_bwd": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p,
                                         _c_void_p, _c_void_p, _c_void_p, _i32, _f32, _c_void_p,
                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p, _sz,
@@ -159,6 +161,22 @@ def qlora_dequant_nf4(packed: torch.Tensor, absmax: torch.Tensor, n_out: int, n_
         out = torch.empty(n_out, n_in, dtype=torch.bfloat16, device=packed.device)
     _check("qlora_dequant_nf4", lib.qlora_dequant_nf4(
         _dev(packed, "packed", torch.uint8), _dev(absmax, "absmax", torch.float32), n_out, n_in,
+        _dev(out, "out", torch.bfloat16), _stream(packed)))
+    return out
+
+
+def qlora_merge_nf4(packed: torch.Tensor, absmax: torch.Tensor, A: torch.Tensor, B: torch.Tensor, s: float,
+                    d_out: int, d_in: int, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Merged weight bf16(W_deq + s . (A . B)^T), [d_out, d_in] bf16."""
+    lib = load_library()
+    r = B.shape[0]
+    if A.shape != (d_in, r) or B.shape != (r, d_out):
+        raise ValueError(f"A must be [{d_in}, r] and B [r, {d_out}], got {tuple(A.shape)}, {tuple(B.shape)}")
+    if out is None:
+        out = torch.empty(d_out, d_in, dtype=torch.bfloat16, device=packed.device)
+    _check("qlora_merge_nf4", lib.qlora_merge_nf4(
+        _dev(packed, "packed", torch.uint8), _dev(absmax, "absmax", torch.float32), d_out, d_in,
+        _dev(A, "A", torch.bfloat16), _dev(B, "B", torch.bfloat16), r, float(s),
         _dev(out, "out", torch.bfloat16), _stream(packed)))
     return out
 

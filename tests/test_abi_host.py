@@ -107,3 +107,13 @@ def test_binding_refuses_cpu_tensors(lib):
     from rank_adapter_linear_nf4_b300 import qlora
     with pytest.raises(ValueError):
         qlora.qlora_quantize_nf4(torch.zeros(4, 64, dtype=torch.bfloat16))
+
+
+def test_merge_argument_validation(lib):
+    def merge(N=256, K=256, r=8, P=FAKE, S=FAKE, A=FAKE, B=FAKE, out=FAKE):
+        return lib.qlora_merge_nf4(P, S, N, K, A, B, r, 1.0, out, None)
+    assert merge(r=0) == 4 and merge(r=129) == 4
+    assert merge(K=100) == 4 and merge(N=252) == 4
+    assert merge(N=0) == 2
+    assert merge(A=None) == 1 and merge(out=None) == 1
+    assert merge(out=MISALIGNED) == 3

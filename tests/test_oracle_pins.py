@@ -308,3 +308,33 @@ def test_scale():
     assert O.lora_scale(32, 16, rank_stabilised=True) == 8.0
     assert O.lora_scale(16, 64, rank_stabilised=True) == pytest.approx(2.0)
     assert math.isclose(O.lora_scale(10, 3, True), 10 / math.sqrt(3))
+
+
+def test_merged_export_with_zero_adapter_is_the_dequantised_weight():
+    """B = 0: the 16-bit export is the bf16 dequantised weight itself, bit for bit."""
+    rng = np.random.default_rng(31)
+    W = O.bf16_round(rng.normal(0.0, 0.02, size=(24, 128)).astype(np.float32))
+    packed, absmax = O.quantize_nf4(W)
+    Wd = O.dequantize_nf4(packed, absmax, 24, 128)
+    A = O.bf16_round(rng.uniform(-0.1, 0.1, size=(128, 8)).astype(np.float32))
+    B = np.zeros((8, 24), dtype=np.float32)
+    out = O.merged_weight_bf16(Wd, A, B, 2.0)
+    assert np.array_equal(O.bf16_bits(out), O.bf16_bits(Wd))
+
+
+def test_merged_export_with_one_hot_adapter_moves_one_column():
+    """A = e_k0 (a single 1 in rank 0), B row 0 = v: only column k0 changes, to
+    bf16(W[:, k0] + s*v), a sum of two exact values rounded once."""
+    rng = np.random.default_rng(32)
+    Wd = O.bf16_round(rng.normal(0.0, 0.02, size=(16, 64)).astype(np.float32))
+    A = np.zeros((64, 4), dtype=np.float32)
+    A[37, 0] = 1.0
+    v = O.bf16_round(rng.normal(0.0, 0.01, size=16).astype(np.float32))
+    B = np.zeros((4, 16), dtype=np.float32)
+    B[0] = v
+    out = O.merged_weight_bf16(Wd, A, B, 0.5)
+    others = np.ones(64, dtype=bool)
+    others[37] = False
+    assert np.array_equal(out[:, others], Wd[:, others])
+    expect = O.bf16_round((Wd[:, 37].astype(np.float64) + 0.5 * v.astype(np.float64)))
+    assert np.array_equal(O.bf16_bits(out[:, 37]), O.bf16_bits(expect))
