@@ -20,6 +20,7 @@ enum KernelKind : int {
   kKindMainFwd,
   kKindMainDx,
   kKindMerge,
+  kKindStream,
   kNumKernelKinds
 };
 
@@ -69,6 +70,9 @@ struct Workspace {
   size_t partial_bytes;
 };
 size_t workspace_bytes(const LayerDims& d);
+// Counters the workspace holds: the main kernel's split tiles (one per SM) or
+// the token-stream kernel's 64-row panels, whichever is more.
+int counter_slots(const LayerDims& d);
 // Bytes of partial tiles the main kernel uses at most for these dimensions.
 size_t split_partial_bytes(const LayerDims& d);
 Workspace carve_workspace(const LayerDims& d, void* base);
@@ -77,9 +81,24 @@ cudaError_t run_forward(const LayerDims& d, const uint16_t* X, const uint8_t* pa
                         const float* absmax, const uint16_t* A, const uint16_t* B, uint16_t* Y,
                         float* XA, const Workspace& ws, int* status, cudaStream_t stream);
 
+// Forward for at most kStreamMaxTokens tokens as a stream of the NF4 weight
+// (lora_stream.cu); it needs counter_slots(d) counters and partial panels for
+// two per CTA in the workspace.
+constexpr int kStreamMaxTokens = 16;
+int stream_counter_slots(const LayerDims& d);
+size_t stream_partial_bytes(int grid);
+bool stream_applies(const LayerDims& d, const Workspace& ws, int sms);
+cudaError_t launch_stream_fwd(const LayerDims& d, const uint16_t* X, const uint8_t* packed, const float* absmax,
+                              const uint16_t* B, const Workspace& ws, uint16_t* Y, int* status, int sms,
+                              cudaStream_t stream);
+
 // Tensor map over a row-major bf16 [rows, cols] matrix, 128-byte swizzle.
 bool make_bf16_map_sw128(CUtensorMap* m, const void* gaddr, uint64_t cols, uint64_t rows, uint32_t box_cols,
                          uint32_t box_rows);
+
+// 2-D tensor map over a row-major [outer, inner] array (row_bytes apart).
+bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* gaddr, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 
 // Merged weight bf16(W_deq + s . (A . B)^T) (lora_merge.cu).
 cudaError_t launch_merge_nf4(const uint8_t* packed, const float* absmax, int N, int K, const uint16_t* A,

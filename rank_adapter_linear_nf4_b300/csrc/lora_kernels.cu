@@ -1198,21 +1198,29 @@ size_t align_up(size_t x) { return (x + 1023) & ~static_cast<size_t>(1023); }
 
 }  // namespace
 
-// Workspace: padded A [K, rp], bf16(s*T) and bf16(s*G) [M, rp], then the main
-// kernel's split-tile counters (one per SM) and partial tiles (two per SM).
+// Workspace: padded A [K, rp], bf16(s*T) and bf16(s*G) [M, rp], then the
+// counters (split tiles of the main kernel, or panels of the token-stream
+// kernel) and the partial tiles (two per SM).
 bool make_bf16_map_sw128(CUtensorMap* m, const void* gaddr, uint64_t cols, uint64_t rows, uint32_t box_cols,
                          uint32_t box_rows) {
   return map_bf16(m, gaddr, cols, rows, box_cols, box_rows, true);
+}
+
+bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* gaddr, uint64_t inner, uint64_t outer,
+                        uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+  return make_map_sw(m, dt, gaddr, inner, outer, row_bytes, box_inner, box_outer, sw);
 }
 
 size_t split_partial_bytes(const LayerDims& d) {
   return static_cast<size_t>(2) * sm_count() * kTileP * pick_bn(d.M) * sizeof(float);
 }
 
+int counter_slots(const LayerDims& d) { return std::max(sm_count(), stream_counter_slots(d)); }
+
 size_t workspace_bytes(const LayerDims& d) {
   const size_t rp = static_cast<size_t>(d.rp);
   return align_up(static_cast<size_t>(d.K) * rp * 2) + 2 * align_up(static_cast<size_t>(d.M) * rp * 2) +
-         align_up(static_cast<size_t>(sm_count()) * sizeof(int)) + align_up(split_partial_bytes(d));
+         align_up(static_cast<size_t>(counter_slots(d)) * sizeof(int)) + align_up(split_partial_bytes(d));
 }
 
 Workspace carve_workspace(const LayerDims& d, void* base) {
@@ -1226,8 +1234,8 @@ Workspace carve_workspace(const LayerDims& d, void* base) {
   w.s_g = reinterpret_cast<uint16_t*>(b);
   b += align_up(static_cast<size_t>(d.M) * rp * 2);
   w.counters = reinterpret_cast<int*>(b);
-  w.counter_cap = sm_count();
-  b += align_up(static_cast<size_t>(sm_count()) * sizeof(int));
+  w.counter_cap = counter_slots(d);
+  b += align_up(static_cast<size_t>(w.counter_cap) * sizeof(int));
   w.partials = reinterpret_cast<float*>(b);
   w.partial_bytes = split_partial_bytes(d);
   return w;
@@ -1262,6 +1270,8 @@ cudaError_t run_forward(const LayerDims& d, const uint16_t* X, const uint8_t* pa
     e = launch_skinny<kRowsT>(d.rp, maps, sp, tiles, pick_split(tiles, sp.num_ct), stream);
     if (e != cudaSuccess) return e;
   }
+  const int sms = sm_count();
+  if (stream_applies(d, ws, sms)) return launch_stream_fwd(d, X, packed, absmax, B, ws, Y, status, sms, stream);
   return launch_main<false>(d, X, ws.s_t, B, d.r, Y, packed, absmax, ws, status, stream);
 }
 

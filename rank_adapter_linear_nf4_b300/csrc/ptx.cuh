@@ -116,6 +116,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, Abort a
   return mbar_wait_slow(bar, parity, ab, honour_abort);
 }
 
+// Waits for the phase by polling test_wait, which never suspends the thread:
+// for pipelines whose stages turn over in well under a microsecond, where the
+// wake-up of a suspended try_wait would set the pace.  Same limit and abort
+// behaviour as mbar_wait.
+static __device__ __noinline__ bool mbar_spin_slow(uint32_t bar, uint32_t parity, Abort ab, bool honour_abort) {
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    for (int i = 0; i < 256; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
+    if (honour_abort && *ab.flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *ab.flag = 1;
+      atomicExch(ab.status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity, Abort ab,
+                                               bool honour_abort = true) {
+#pragma unroll 1
+  for (int i = 0; i < 32; ++i)
+    if (mbar_test_wait(bar, parity)) return true;
+  return mbar_spin_slow(bar, parity, ab, honour_abort);
+}
+
 // ---------------------------------------------------------------- proxies / fences
 
 // Make this thread's generic-proxy shared-memory writes visible to the async

@@ -86,7 +86,7 @@ std::vector<cudaEvent_t> g_free_events;
 
 const char* const kKindNames[qlora::kNumKernelKinds] = {
     "nf4_quantize", "nf4_dequant", "lora_pad_A", "lora_rows_T", "lora_rows_G",
-    "lora_red_dA_dB", "lora_main_fwd", "lora_main_dX", "lora_merge"};
+    "lora_red_dA_dB", "lora_main_fwd", "lora_main_dX", "lora_merge", "lora_stream_fwd"};
 
 cudaEvent_t take_event() {
   if (!g_free_events.empty()) {

@@ -14,6 +14,7 @@
 // ordering between them) race on it; serialise them on one stream.  Every
 // byte a call reads from the array is written earlier in the same call, so
 // the contents left by the previous call never need clearing.
+#include <algorithm>
 #include <cstddef>
 #include <cstdint>
 #include <mutex>
@@ -101,12 +102,14 @@ extern "C" qlora_status qlora_linear_fwd_noalloc(const uint16_t* X, int64_t M, i
   ws.a_pad = static_cast<uint16_t*>(scratch);
   ws.s_t = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(scratch) + a_pad_bytes);
   ws.s_g = nullptr;   // backward only
-  // what is left of the array holds the split-tile counters and partial tiles
-  // of the main kernel; when they do not fit it takes whole tiles only
+  // what is left of the array holds the counters and partial tiles of the
+  // main kernel and the token-stream kernel; without them the main kernel
+  // takes whole tiles only
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const size_t counter_bytes = round_up_1k(static_cast<size_t>(sms) * sizeof(int));
+  const int n_counters = std::max(sms, qlora::stream_counter_slots(d));
+  const size_t counter_bytes = round_up_1k(static_cast<size_t>(n_counters) * sizeof(int));
   const size_t used = a_pad_bytes + s_t_bytes;
   ws.counters = nullptr;
   ws.counter_cap = 0;
@@ -115,7 +118,7 @@ extern "C" qlora_status qlora_linear_fwd_noalloc(const uint16_t* X, int64_t M, i
   if (sms > 0 && used + counter_bytes < kNoAllocScratchBytes) {
     uint8_t* rest = static_cast<uint8_t*>(scratch) + used;
     ws.counters = reinterpret_cast<int*>(rest);
-    ws.counter_cap = sms;
+    ws.counter_cap = n_counters;
     ws.partials = reinterpret_cast<float*>(rest + counter_bytes);
     ws.partial_bytes = kNoAllocScratchBytes - used - counter_bytes;
   }
