@@ -12,7 +12,10 @@
 //     one CTA per SM.  A producer warp streams a CTA's stages through a ring of
 //     shared-memory slots with TMA (codes, absmax, and the matching columns of
 //     X), several stages ahead; sixteen consumer warps each take 32 features
-//     of every stage for 32 of its 64 rows.
+//     of every stage for 32 of its 64 rows.  With at least as many 64-row
+//     panels as CTAs each CTA takes whole panels (at most one panel of
+//     imbalance, and no partial sums between CTAs); with fewer, the stages are
+//     split evenly and a panel may be shared by CTAs.
 //   * Every consumer thread decodes its share of the codes straight into the
 //     register operands of mma.sync (m16n8k16, bf16 -> fp32): one shared-memory
 //     lookup per code byte in a 256-entry table of bf16 code pairs (one copy per
@@ -93,6 +96,7 @@ struct StreamParams {
   int M, N, r, rp;
   int units;                // stages per panel: K / 256
   long long total;          // panels * units
+  int whole;                // 1: every CTA takes whole panels (panels >= CTAs)
 };
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -260,7 +264,11 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int G = gridDim.x, cta = blockIdx.x;
-  const long long u_begin = p.total * cta / G, u_end = p.total * (cta + 1) / G;
+  // whole panels when there are at least as many panels as CTAs (no panel is
+  // split, so no partials); otherwise the stages are split evenly
+  const long long panels = p.total / p.units;
+  const long long u_begin = p.whole ? panels * cta / G * p.units : p.total * cta / G;
+  const long long u_end = p.whole ? panels * (cta + 1) / G * p.units : p.total * (cta + 1) / G;
   const int n_stages = static_cast<int>(u_end - u_begin);
   Abort ab{&s_abort, p.status};
 
@@ -385,8 +393,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
     }
     named_bar_sync(kNamedBar, kConsumers);
 
-    const int first_c = owner_cta(pu0, p.total, G);
-    const int last_c = owner_cta(pu0 + p.units - 1, p.total, G);
+    const int first_c = p.whole ? cta : owner_cta(pu0, p.total, G);
+    const int last_c = p.whole ? cta : owner_cta(pu0 + p.units - 1, p.total, G);
     constexpr int kOut = kPanelRows * 8 * MT;
     if (first_c == last_c) {
       // the whole panel is this CTA's: sum the warps in order and store
@@ -503,7 +511,9 @@ cudaError_t launch_stream_fwd(const LayerDims& d, const uint16_t* X, const uint8
   p.r = d.r;
   p.rp = d.rp;
   p.units = d.K / kStageK;
-  p.total = static_cast<long long>(stream_counter_slots(d)) * p.units;
+  const int panels = stream_counter_slots(d);
+  p.total = static_cast<long long>(panels) * p.units;
+  p.whole = panels >= sms ? 1 : 0;
   const int grid = static_cast<int>(p.total < sms ? p.total : sms);
   if (mt == 1) return launch_stream_mt<1>(maps, p, grid, stream);
   return launch_stream_mt<2>(maps, p, grid, stream);

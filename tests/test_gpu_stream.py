@@ -1,10 +1,11 @@
 """The forward for 1..16 tokens (the NF4 weight-stream kernel) against the oracle.
 
 Same bar as the other layer tests: per output tensor, max|gpu - oracle| <=
-1e-2 * max|oracle|, every element compared.  The cases walk the kernel's
-schedule: panels of 64 weight rows with a ragged last one, a panel split over
-many CTAs (each CTA one unit), whole panels inside one CTA next to split
-ones, one and two low-rank units per panel, token counts on both sides of 8.
+1e-2 * max|oracle|, every element compared.  The cases walk the kernel's two
+schedules: whole 64-row panels per CTA (at least as many panels as SMs, the
+last panel ragged) and stages split evenly with panels shared by CTAs (a
+panel over many CTAs, each one stage; whole panels inside one CTA next to
+split ones); ranks 1..128 and token counts on both sides of 8.
 Low-rank-dominant cases (zero base weight, B ~ N(0, 1)) check that term on its
 own, since with the standard scales it is only a few percent of Y.
 """
@@ -34,6 +35,7 @@ CASES = [
     (16, 4096, 4096, 16, 1.0),      # the q_proj layer at 16 tokens
     (12, 512, 200, 65, 1.25),       # rank padded to 128, A padded (r % 8 != 0), last panel 8 rows
     (2, 256, 8, 1, 3.0),            # one 8-row panel, rank 1
+    (4, 1024, 64 * 148 + 8, 16, 0.5),   # 149 panels, whole panels per CTA, the last one 8 rows
 ]
 
 
