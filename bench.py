@@ -471,7 +471,7 @@ def run_ours(args):
         "kernels": per_kernel,
         "profiled_ms_per_step": prof_total_ms / args.steps,
         "gpu_launches": launches,
-        "nf4_codec": codec,
+        "hbm_kernels": codec,
         "cuda_graph": graph,
         "clocks": clocks,
         "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
@@ -511,8 +511,11 @@ def graph_timing(step, n_sets, flops, world, timed, replays=20):
 
 
 def codec_rooflines(sh, sets, dev, peaks, stream, reps=20):
-    """NF4 quantise and dequantise of this workload's weight (rows a1, a2), timed
-    alone with CUDA events, alternating two weights (> L2 together); HBM-bound."""
+    """The HBM-bound kernels beside the layer, each timed alone with CUDA events,
+    alternating two inputs (> L2 together): NF4 quantise and dequantise of this
+    workload's weight (rows a1, a2), the merged weight bf16(W_deq + s.(A.B)^T)
+    (the merge export), and the SwiGLU gate and its backward at [M, d_out]
+    (the gate between a stacked gate/up layer of this width and a down layer)."""
     import torch
     from rank_adapter_linear_nf4_b300 import qlora
     n = sh.d_in * sh.d_out
@@ -520,13 +523,26 @@ def codec_rooflines(sh, sets, dev, peaks, stream, reps=20):
     outs = [torch.empty_like(w) for w in Ws]
     pk = [torch.empty_like(t["packed"]) for t in sets[:2]]
     am = [torch.empty_like(t["absmax"]) for t in sets[:2]]
+    g = torch.Generator(device=dev).manual_seed(5)
+    gus = [torch.randn(sh.M, 2 * sh.d_out, device=dev, generator=g).to(torch.bfloat16) for _ in range(2)]
+    dhs = [torch.randn(sh.M, sh.d_out, device=dev, generator=g).to(torch.bfloat16) for _ in range(2)]
+    hs = [torch.empty_like(d) for d in dhs]
+    dgus = [torch.empty_like(x) for x in gus]
+    m_ff = sh.M * sh.d_out
     res = {}
-    for name, fn, nbytes in (
+    for name, fn, nbytes, elems in (
             ("nf4_quantize", lambda i: qlora.qlora_quantize_nf4(Ws[i % 2], packed=pk[i % 2], absmax=am[i % 2]),
-             2.0 * n + 0.5 * n + n / 16.0),
+             2.0 * n + 0.5 * n + n / 16.0, n),
             ("nf4_dequant", lambda i: qlora.qlora_dequant_nf4(sets[i % 2]["packed"], sets[i % 2]["absmax"],
                                                               sh.d_out, sh.d_in, out=outs[i % 2]),
-             0.5 * n + n / 16.0 + 2.0 * n)):
+             0.5 * n + n / 16.0 + 2.0 * n, n),
+            ("lora_merge", lambda i: qlora.qlora_merge_nf4(sets[i % 2]["packed"], sets[i % 2]["absmax"],
+                                                           sets[i % 2]["A"], sets[i % 2]["B"], sh.s, sh.d_out,
+                                                           sh.d_in, out=outs[i % 2]),
+             0.5 * n + n / 16.0 + 2.0 * n + 2.0 * sh.r * (sh.d_in + sh.d_out), n),
+            ("swiglu_fwd", lambda i: qlora.qlora_swiglu_fwd(gus[i % 2], out=hs[i % 2]), 6.0 * m_ff, m_ff),
+            ("swiglu_bwd", lambda i: qlora.qlora_swiglu_bwd(gus[i % 2], dhs[i % 2], out=dgus[i % 2]),
+             10.0 * m_ff, m_ff)):
         for i in range(3):
             fn(i)
         torch.cuda.synchronize()
@@ -543,7 +559,7 @@ def codec_rooflines(sh, sets, dev, peaks, stream, reps=20):
         gbs = nbytes / (us * 1e-6) / 1e9
         res[name] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm"], "avg_launch_us": us,
-                     "algorithmic_bytes_per_launch": nbytes, "elements": n}
+                     "algorithmic_bytes_per_launch": nbytes, "elements": elems}
     return res
 
 

@@ -139,6 +139,28 @@ qlora_status qlora_merge_nf4(const uint8_t* packed, const float* absmax, int64_t
                              const uint16_t* A, const uint16_t* B, int32_t r, float s, uint16_t* W_out,
                              qlora_stream_t stream);
 
+/*
+ * SwiGLU gate of the MLP block, between the stacked gate/up projection and the
+ * down projection (the pages fuse the MLP into their forward: "Unsloth性能实测：
+ * 比传统方法快2倍真的吗？", section 2.2; SwiGLU is among the fused transformer
+ * operators of "UnSloth加速原理：CUDA内核融合与内存优化", section "在ms-swift中的角色"):
+ *   h[m, j] = bf16_rne(silu(g) * u),  g = gu[m, j], u = gu[m, d_ff + j],
+ *   silu(x) = x / (1 + e^-x), fp32 arithmetic.
+ *   gu [M, 2*d_ff] bf16 (gate columns, then up columns), read;  h [M, d_ff] bf16, written.
+ * Requires M >= 0 (0 launches nothing), d_ff % 8 == 0; gu and h 16-byte aligned.
+ */
+qlora_status qlora_swiglu_fwd(const uint16_t* gu, int64_t M, int64_t d_ff, uint16_t* h, qlora_stream_t stream);
+
+/*
+ * Its backward, written in the layout of gu (the dY of the stacked projection):
+ *   dgu[m, j]        = bf16_rne(dh * u * sigma(g) * (1 + g * (1 - sigma(g))))   (d/dg)
+ *   dgu[m, d_ff + j] = bf16_rne(dh * silu(g))                                   (d/du)
+ *   gu [M, 2*d_ff] and dh [M, d_ff] bf16, read;  dgu [M, 2*d_ff] bf16, written.
+ * Same requirements as qlora_swiglu_fwd (gu, dh, dgu 16-byte aligned).
+ */
+qlora_status qlora_swiglu_bwd(const uint16_t* gu, const uint16_t* dh, int64_t M, int64_t d_ff, uint16_t* dgu,
+                              qlora_stream_t stream);
+
 /* Bytes of scratch qlora_linear_fwd / qlora_linear_bwd need for this shape
  * (0 if the shape is unsupported).  The same workspace serves both calls. */
 size_t qlora_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int32_t r);

@@ -21,6 +21,8 @@ enum KernelKind : int {
   kKindMainDx,
   kKindMerge,
   kKindStream,
+  kKindSwigluFwd,
+  kKindSwigluBwd,
   kNumKernelKinds
 };
 
@@ -99,6 +101,12 @@ bool make_bf16_map_sw128(CUtensorMap* m, const void* gaddr, uint64_t cols, uint6
 // 2-D tensor map over a row-major [outer, inner] array (row_bytes apart).
 bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* gaddr, uint64_t inner, uint64_t outer,
                         uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+
+// SwiGLU gate of the MLP block (swiglu.cu): h = silu(g) * u from the stacked
+// gate/up output gu [rows, 2*d_ff], and its backward into dgu (same layout).
+cudaError_t launch_swiglu_fwd(const uint16_t* gu, int64_t rows, int64_t d_ff, uint16_t* h, cudaStream_t stream);
+cudaError_t launch_swiglu_bwd(const uint16_t* gu, const uint16_t* dh, int64_t rows, int64_t d_ff, uint16_t* dgu,
+                              cudaStream_t stream);
 
 // Merged weight bf16(W_deq + s . (A . B)^T) (lora_merge.cu).
 cudaError_t launch_merge_nf4(const uint8_t* packed, const float* absmax, int N, int K, const uint16_t* A,

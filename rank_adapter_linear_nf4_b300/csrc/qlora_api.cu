@@ -86,7 +86,7 @@ std::vector<cudaEvent_t> g_free_events;
 
 const char* const kKindNames[qlora::kNumKernelKinds] = {
     "nf4_quantize", "nf4_dequant", "lora_pad_A", "lora_rows_T", "lora_rows_G",
-    "lora_red_dA_dB", "lora_main_fwd", "lora_main_dX", "lora_merge", "lora_stream_fwd"};
+    "lora_red_dA_dB", "lora_main_fwd", "lora_main_dX", "lora_merge", "lora_stream_fwd", "swiglu_fwd", "swiglu_bwd"};
 
 cudaEvent_t take_event() {
   if (!g_free_events.empty()) {
@@ -244,6 +244,36 @@ qlora_status qlora_merge_nf4(const uint8_t* packed, const float* absmax, int64_t
   if (status == nullptr) return cuda_fail(static_cast<cudaError_t>(cuda_error));
   cudaError_t e = qlora::launch_merge_nf4(packed, absmax, static_cast<int>(d_out), static_cast<int>(d_in), A, B, r,
                                           s, W_out, status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+namespace {
+qlora_status check_swiglu(int64_t M, int64_t d_ff) {
+  if (M < 0 || d_ff < 1) return QLORA_ERR_SHAPE;
+  if (d_ff > (int64_t(1) << 30) || (M > 0 && M > (int64_t(1) << 40) / d_ff)) return QLORA_ERR_SHAPE;
+  if (d_ff % 8 != 0) return QLORA_ERR_UNSUPPORTED;
+  return QLORA_OK;
+}
+}  // namespace
+
+qlora_status qlora_swiglu_fwd(const uint16_t* gu, int64_t M, int64_t d_ff, uint16_t* h, qlora_stream_t stream) {
+  const qlora_status st = check_swiglu(M, d_ff);
+  if (st != QLORA_OK) return st;
+  if (M == 0) return QLORA_OK;
+  if (!gu || !h) return QLORA_ERR_NULL;
+  if (!aligned16(gu) || !aligned16(h)) return QLORA_ERR_ALIGN;
+  cudaError_t e = qlora::launch_swiglu_fwd(gu, M, d_ff, h, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+qlora_status qlora_swiglu_bwd(const uint16_t* gu, const uint16_t* dh, int64_t M, int64_t d_ff, uint16_t* dgu,
+                              qlora_stream_t stream) {
+  const qlora_status st = check_swiglu(M, d_ff);
+  if (st != QLORA_OK) return st;
+  if (M == 0) return QLORA_OK;
+  if (!gu || !dh || !dgu) return QLORA_ERR_NULL;
+  if (!aligned16(gu) || !aligned16(dh) || !aligned16(dgu)) return QLORA_ERR_ALIGN;
+  cudaError_t e = qlora::launch_swiglu_bwd(gu, dh, M, d_ff, dgu, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
 }
 

@@ -44,6 +44,8 @@ _SIGNATURES = {
                                                 _c_void_p]),
     "qlora_merge_nf4": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p, _i32, _f32,
                                        _c_void_p, _c_void_p]),
+    "qlora_swiglu_fwd": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
+    "qlora_swiglu_bwd": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
     "qlora_linear_bwd": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p,
                                         _c_void_p, _c_void_p, _c_void_p, _i32, _f32, _c_void_p,
                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p, _sz,
@@ -178,6 +180,33 @@ def qlora_merge_nf4(packed: torch.Tensor, absmax: torch.Tensor, A: torch.Tensor,
         _dev(packed, "packed", torch.uint8), _dev(absmax, "absmax", torch.float32), d_out, d_in,
         _dev(A, "A", torch.bfloat16), _dev(B, "B", torch.bfloat16), r, float(s),
         _dev(out, "out", torch.bfloat16), _stream(packed)))
+    return out
+
+
+def qlora_swiglu_fwd(gu: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """h = silu(g) * u from the stacked gate/up output gu [M, 2*d_ff] -> [M, d_ff] bf16."""
+    lib = load_library()
+    M, two = gu.shape
+    d_ff = two // 2
+    if out is None:
+        out = torch.empty(M, d_ff, dtype=torch.bfloat16, device=gu.device)
+    _check("qlora_swiglu_fwd", lib.qlora_swiglu_fwd(
+        _dev(gu, "gu", torch.bfloat16), M, d_ff, _dev(out, "h", torch.bfloat16), _stream(gu)))
+    return out
+
+
+def qlora_swiglu_bwd(gu: torch.Tensor, dh: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """[d/dg | d/du] of h = silu(g) * u, in the layout of gu [M, 2*d_ff] bf16."""
+    lib = load_library()
+    M, two = gu.shape
+    d_ff = two // 2
+    if dh.shape != (M, d_ff):
+        raise ValueError(f"dh must be [{M}, {d_ff}], got {tuple(dh.shape)}")
+    if out is None:
+        out = torch.empty(M, 2 * d_ff, dtype=torch.bfloat16, device=gu.device)
+    _check("qlora_swiglu_bwd", lib.qlora_swiglu_bwd(
+        _dev(gu, "gu", torch.bfloat16), _dev(dh, "dh", torch.bfloat16), M, d_ff,
+        _dev(out, "dgu", torch.bfloat16), _stream(gu)))
     return out
 
 

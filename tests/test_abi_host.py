@@ -117,3 +117,16 @@ def test_merge_argument_validation(lib):
     assert merge(N=0) == 2
     assert merge(A=None) == 1 and merge(out=None) == 1
     assert merge(out=MISALIGNED) == 3
+
+
+def test_swiglu_argument_validation(lib):
+    def fwd(M=4, d_ff=64, gu=FAKE, h=FAKE):
+        return lib.qlora_swiglu_fwd(gu, M, d_ff, h, None)
+
+    def bwd(M=4, d_ff=64, gu=FAKE, dh=FAKE, dgu=FAKE):
+        return lib.qlora_swiglu_bwd(gu, dh, M, d_ff, dgu, None)
+    assert fwd(d_ff=12) == 4 and bwd(d_ff=12) == 4
+    assert fwd(d_ff=0) == 2 and fwd(M=-1) == 2 and bwd(d_ff=0) == 2
+    assert fwd(gu=None) == 1 and bwd(dh=None) == 1 and bwd(dgu=None) == 1
+    assert fwd(h=MISALIGNED) == 3 and bwd(gu=MISALIGNED) == 3
+    assert fwd(M=0, gu=None, h=None) == 0 and bwd(M=0, gu=None, dh=None, dgu=None) == 0

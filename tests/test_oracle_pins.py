@@ -338,3 +338,40 @@ def test_merged_export_with_one_hot_adapter_moves_one_column():
     assert np.array_equal(out[:, others], Wd[:, others])
     expect = O.bf16_round((Wd[:, 37].astype(np.float64) + 0.5 * v.astype(np.float64)))
     assert np.array_equal(O.bf16_bits(out[:, 37]), O.bf16_bits(expect))
+
+
+# ---- SwiGLU gate of the MLP block ------------------------------------------
+
+def test_swiglu_forward_against_library_sigmoid():
+    """h = g * sigma(g) * u with scipy's expit as sigma, and closed-form values."""
+    from scipy.special import expit
+    rng = np.random.default_rng(7)
+    gu = rng.normal(0.0, 3.0, size=(5, 16))
+    g, u = gu[:, :8], gu[:, 8:]
+    np.testing.assert_allclose(O.swiglu_forward(gu), g * expit(g) * u, rtol=1e-14, atol=1e-300)
+    one = np.array([[0.0, 1.0, 40.0, -40.0, 1.0, 1.0, 1.0, 1.0]])
+    h = O.swiglu_forward(one)[0]
+    assert h[0] == 0.0                                        # silu(0) = 0
+    assert abs(h[1] - 1.0 / (1.0 + np.exp(-1.0))) < 1e-15     # silu(1) = sigma(1)
+    assert abs(h[2] - 40.0) < 1e-12 and abs(h[3]) < 1e-15     # saturation at both ends
+
+
+def test_swiglu_gate_is_the_first_half():
+    gu = np.array([[2.0, 3.0]])
+    assert O.swiglu_forward(gu)[0, 0] == 2.0 / (1.0 + np.exp(-2.0)) * 3.0
+    assert O.swiglu_forward(gu[:, ::-1])[0, 0] == 3.0 / (1.0 + np.exp(-3.0)) * 2.0
+
+
+def test_swiglu_backward_matches_finite_differences():
+    rng = np.random.default_rng(8)
+    gu = rng.normal(0.0, 2.0, size=(3, 12))
+    dh = rng.normal(0.0, 1.0, size=(3, 6))
+    grad = O.swiglu_backward(gu, dh)
+    eps = 1e-6
+    num = np.zeros_like(gu)
+    for idx in np.ndindex(gu.shape):
+        p, m = gu.copy(), gu.copy()
+        p[idx] += eps
+        m[idx] -= eps
+        num[idx] = np.sum((O.swiglu_forward(p) - O.swiglu_forward(m)) * dh) / (2 * eps)
+    np.testing.assert_allclose(grad, num, rtol=1e-7, atol=1e-9)
