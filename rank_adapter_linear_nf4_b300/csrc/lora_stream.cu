@@ -30,10 +30,14 @@
 //   * The contraction order inside an MMA is free: thread (g, c) of the MMA
 //     takes 8 consecutive features (one 32-bit word of codes per row) and the
 //     activations are read in the same permuted order.
-//   * The low-rank term s*T.B of a panel is added by the CTA that holds the
-//     panel's first stage: it copies the panel's columns of B and bf16(s*T) into
-//     shared memory (cp.async) while its stages stream, then four warps multiply
-//     them (ldmatrix.trans + mma) into the panel partial.
+//   * The decode table is a compile-time array in global memory, copied into
+//     shared memory by one bulk copy while the first stages load.
+//   * At the end of a panel segment the consumers leave their partials in
+//     shared memory and go on; four epilogue warps (one per 16-row group) sum
+//     them, add the low-rank term s*T.B when the CTA holds the panel's first
+//     stage (B and bf16(s*T) copied in with cp.async, multiplied with
+//     ldmatrix.trans + mma), and write the panel, overlapping the next
+//     segment's stages.
 //   * A panel split between CTAs is finished by the last of them to arrive (a
 //     counter per panel, zeroed by the rank-r kernel that runs before this one):
 //     it adds the fp32 partials in CTA order, so the result does not depend on
@@ -44,6 +48,7 @@
 
 #include <cuda_bf16.h>
 #include <cstdint>
+#include <cstring>
 
 #include "kernels.h"
 #include "nf4_lut.cuh"
@@ -55,7 +60,11 @@ namespace {
 constexpr int kSlices = 8;                         // 32-feature slices of a stage
 constexpr int kConsumerWarps = 2 * kSlices;        // each slice for the upper and the lower 32 rows
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kStreamThreads = kConsumers + 32;   // + the producer warp
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kEpilogueWarps = 4;                  // one per 16-row group of a panel
+constexpr int kEpilogueWarp0 = kConsumerWarps + 1;
+constexpr int kEpilogueThreads = kEpilogueWarps * 32;
+constexpr int kStreamThreads = kConsumers + 32 + kEpilogueThreads;
 constexpr int kPanelRows = 64;                     // weight rows per panel (4 MMA row groups)
 constexpr int kStageK = 256;                       // input features per stage (4 NF4 blocks)
 constexpr int kSlotStride = kPanelRows + 4;        // fp32 per token row of a warp's panel partial
@@ -64,7 +73,30 @@ constexpr int kPartialFloats = 16 * kPanelRows;    // one panel partial in globa
 constexpr int kLutWords = 256 * 32;                // 256 code bytes x 32 lane copies
 constexpr int kBsStride = 64 * 2 + 16;             // bytes per rank row of the panel's B columns
 constexpr int kTsStride = 128 * 2 + 16;            // bytes per token row of bf16(s*T)
-constexpr int kNamedBar = 1;                       // consumer-only barrier
+constexpr int kEpiBar = 1;                         // epilogue-warps-only barrier
+
+// bf16 bit patterns (round to nearest even) of the NF4 levels, in code order:
+// the host copy kNF4LevelsHost rounded; launch_stream_fwd checks the two agree.
+constexpr uint16_t kLevelBf16[16] = {0xBF80, 0xBF32, 0xBF06, 0xBECA, 0xBE92, 0xBE3D, 0xBDBA, 0x0000,
+                                     0x3DA3, 0x3E25, 0x3E7C, 0x3EAD, 0x3EE2, 0x3F10, 0x3F39, 0x3F80};
+
+// The decode table: word 32 * v + l (l = lane copy) holds, for code byte v,
+// bf16(level[v >> 4]) (the byte's first element) in the low half and
+// bf16(level[v & 15]) in the high half.
+struct alignas(16) PairTable {
+  uint32_t w[kLutWords];
+};
+
+constexpr PairTable make_pair_table() {
+  PairTable t{};
+  for (int i = 0; i < kLutWords; ++i) {
+    const int v = i >> 5;
+    t.w[i] = static_cast<uint32_t>(kLevelBf16[v >> 4]) | (static_cast<uint32_t>(kLevelBf16[v & 15]) << 16);
+  }
+  return t;
+}
+
+__device__ const PairTable g_pair_table = make_pair_table();
 
 // Shared memory: the ring (1024-aligned for the 128-byte swizzle), then the
 // decode table, the warps' panel partials, the low-rank operands, the barriers.
@@ -81,7 +113,7 @@ struct StreamSmem {
   static constexpr int kBsOffset = kSlotOffset + kSlices * kSlotFloats * 4;
   static constexpr int kTsOffset = kBsOffset + 128 * kBsStride;
   static constexpr int kBarOffset = kTsOffset + 16 * kTsStride;
-  static constexpr int kBytes = kBarOffset + 16 * kStages + 1024;   // + alignment slack
+  static constexpr int kBytes = kBarOffset + 16 * kStages + 32 + 1024;   // + table/slot barriers, slack
   static_assert(kStageBytes % 1024 == 0, "stages keep the swizzle alignment");
   static_assert(kBytes <= 227 * 1024, "fits the shared memory of one CTA");
 };
@@ -188,9 +220,9 @@ __device__ __forceinline__ void consume_stage(const uint8_t* st, const uint8_t* 
   }
 }
 
-// The panel's B columns [rp][64] -> shared memory, by the consumers.
-__device__ __forceinline__ void stage_lowrank_b(const StreamParams& p, int n0, uint32_t bs, int t) {
-  for (int e = t; e < p.rp * 8; e += kConsumers) {
+// The panel's B columns [rp][64] -> shared memory, by the epilogue warps (et = 0..127).
+__device__ __forceinline__ void stage_lowrank_b(const StreamParams& p, int n0, uint32_t bs, int et) {
+  for (int e = et; e < p.rp * 8; e += kEpilogueThreads) {
     const int j = e >> 3, q = e & 7, n = n0 + 8 * q;
     const bool ok = j < p.r && n < p.N;
     cp_async16(bs + j * kBsStride + q * 16,
@@ -199,12 +231,12 @@ __device__ __forceinline__ void stage_lowrank_b(const StreamParams& p, int n0, u
   cp_async_commit();
 }
 
-// bf16(s*T) [8*MT tokens][rp] -> shared memory, by one warp (after it waits for
-// the kernel that writes it).
+// bf16(s*T) [8*MT tokens][rp] -> shared memory, by the epilogue warps (after
+// they wait for the kernel that writes it).
 template <int MT>
-__device__ __forceinline__ void stage_lowrank_t(const StreamParams& p, uint32_t ts, int lane) {
+__device__ __forceinline__ void stage_lowrank_t(const StreamParams& p, uint32_t ts, int et) {
   const int chunks = p.rp / 8;
-  for (int e = lane; e < MT * 8 * chunks; e += 32) {
+  for (int e = et; e < MT * 8 * chunks; e += kEpilogueThreads) {
     const int tok = e / chunks, q = e % chunks;
     const bool ok = tok < p.M;
     cp_async16(ts + tok * kTsStride + q * 16,
@@ -212,37 +244,6 @@ __device__ __forceinline__ void stage_lowrank_t(const StreamParams& p, uint32_t 
                ok ? 16u : 0u);
   }
   cp_async_commit();
-}
-
-// Row group g (panel rows 16g .. 16g+15) of the low-rank term, added to the
-// warp's partial panel in shared memory ([token][row]).
-template <int MT>
-__device__ __forceinline__ void lowrank_group(const StreamParams& p, uint32_t bs, uint32_t ts, float* slot, int g,
-                                              int lane) {
-  const int g4 = lane >> 2, c = lane & 3;
-  float d[MT][4];
-#pragma unroll
-  for (int j = 0; j < MT; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.f;
-  const int mi = lane >> 3, rr = lane & 7;
-  for (int ks = 0; ks < p.rp / 16; ++ks) {
-    uint32_t a[4];
-    const int jr = 16 * ks + rr + ((mi & 2) ? 8 : 0);
-    const int nc = 16 * g + ((mi & 1) ? 8 : 0);
-    ldmatrix_x4_trans(a, bs + jr * kBsStride + nc * 2);
-#pragma unroll
-    for (int j = 0; j < MT; ++j) {
-      const uint32_t row = ts + (8 * j + g4) * kTsStride + (16 * ks + 2 * c) * 2;
-      mma_16816(d[j], a, lds32(row), lds32(row + 16));
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < MT; ++j) {
-    const int row = 16 * g + g4, tok = 8 * j + 2 * c;
-    slot[tok * kSlotStride + row] += d[j][0];
-    slot[(tok + 1) * kSlotStride + row] += d[j][1];
-    slot[tok * kSlotStride + row + 8] += d[j][2];
-    slot[(tok + 1) * kSlotStride + row + 8] += d[j][3];
-  }
 }
 
 __device__ __forceinline__ int owner_cta(long long x, long long total, int G) {
@@ -259,8 +260,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const gbase = smem_raw + (base - smem_u32(smem_raw));
   const uint32_t bar_full = base + S::kBarOffset, bar_empty = bar_full + 8 * S::kStages;
+  const uint32_t bar_table = bar_empty + 8 * S::kStages;
+  const uint32_t bar_slots_full = bar_table + 8, bar_slots_free = bar_table + 16;
   float* const slots = reinterpret_cast<float*>(gbase + S::kSlotOffset);
-  const uint32_t bs = base + S::kBsOffset, ts = base + S::kTsOffset;
 
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int G = gridDim.x, cta = blockIdx.x;
@@ -272,25 +274,28 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
   const int n_stages = static_cast<int>(u_end - u_begin);
   Abort ab{&s_abort, p.status};
 
-  // the table: entry v holds bf16(level[v >> 4]) (first element) and bf16(level[v & 15])
-  uint32_t* const lut = reinterpret_cast<uint32_t*>(gbase + S::kLutOffset);
-  for (int i = t; i < kLutWords; i += kStreamThreads) {
-    const int v = i >> 5;
-    lut[i] = pack_bf16x2(c_nf4_level[v >> 4], c_nf4_level[v & 15]);
-  }
   if (t == 0) {
     s_abort = 0;
     for (int i = 0; i < S::kStages; ++i) {
       mbar_init(bar_full + 8 * i, 1);
       mbar_init(bar_empty + 8 * i, kConsumerWarps);
     }
+    mbar_init(bar_table, 1);
+    mbar_init(bar_slots_full, kConsumerWarps);
+    mbar_init(bar_slots_free, kEpilogueWarps);
     fence_barrier_init();
   }
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
-    // ---- producer: codes, absmax and X columns of each stage, kStages ahead
+  if (warp == kProducerWarp) {
+    // ---- producer: the decode table, then codes, absmax and X columns of each
+    //      stage, kStages ahead
     if (lane == 0) {
+      const uint32_t table = base + S::kLutOffset;
+      mbar_arrive_expect_tx(bar_table, kLutWords * 4);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        bulk_load_1d(table + q * (kLutWords / 4) * 4, g_pair_table.w + q * (kLutWords / 4), kLutWords, bar_table);
       tma_prefetch_map(&map_codes);
       tma_prefetch_map(&map_abs);
       tma_prefetch_map(&map_x);
@@ -310,41 +315,132 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         tma_load_2d(st + S::kAbsOffset, &map_abs, full, q * 4, panel * kPanelRows);
       }
       // no copy may still be landing when the CTA exits
+      mbar_wait(bar_table, 0, ab, false);
       for (int k = i - 1; k >= 0 && k >= i - S::kStages; --k)
         mbar_wait(bar_full + 8 * (k % S::kStages), (k / S::kStages) & 1, ab, false);
     }
     return;
   }
 
-  // ---- consumers
   const int g4 = lane >> 2, c = lane & 3;
+
+  if (warp >= kEpilogueWarp0) {
+    // ---- epilogue: warp ew takes row group ew of every panel segment, behind the consumers
+    const int ew = warp - kEpilogueWarp0, et = t - kEpilogueWarp0 * 32;
+    const uint32_t bs = base + S::kBsOffset, ts = base + S::kTsOffset;
+    const int first_panel = static_cast<int>(u_begin / p.units);
+    bool waited = false;
+    int k = 0;   // segment index within the CTA
+    for (long long seg = u_begin; seg < u_end; ++k) {
+      const int panel = static_cast<int>(seg / p.units);
+      const long long pu0 = static_cast<long long>(panel) * p.units;
+      const long long seg_end = u_end < pu0 + p.units ? u_end : pu0 + p.units;
+      const int n0 = panel * kPanelRows;
+      const bool lowrank = seg == pu0;   // this CTA holds the panel's first stage
+      if (lowrank) {
+        stage_lowrank_b(p, n0, bs, et);
+        if (!waited) {
+          griddep_wait();   // bf16(s*T) and the counters come from the kernel before this one
+          waited = true;
+        }
+        stage_lowrank_t<MT>(p, ts, et);
+      }
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(bar_slots_full, k & 1, ab));
+      // the eight slices' partials of this warp's 16 rows
+      float acc[MT][4];
+#pragma unroll
+      for (int j = 0; j < MT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int at = (8 * j + 2 * c + (e & 1)) * kSlotStride + 16 * ew + g4 + 8 * (e >> 1);
+          float sum = 0.f;
+#pragma unroll
+          for (int b = 0; b < kSlices; ++b) sum += slots[b * kSlotFloats + at];
+          acc[j][e] = sum;
+        }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_slots_free);   // the consumers may write the next segment's partials
+      if (lowrank) {
+        cp_async_wait_all();
+        named_bar_sync(kEpiBar, kEpilogueThreads);   // every copy of B and bf16(s*T) has landed
+        const int mi = lane >> 3, rr = lane & 7;
+        for (int ks = 0; ks < p.rp / 16; ++ks) {
+          uint32_t a[4];
+          ldmatrix_x4_trans(a, bs + (16 * ks + rr + ((mi & 2) ? 8 : 0)) * kBsStride +
+                                   (16 * ew + ((mi & 1) ? 8 : 0)) * 2);
+#pragma unroll
+          for (int j = 0; j < MT; ++j) {
+            const uint32_t row = ts + (8 * j + g4) * kTsStride + (16 * ks + 2 * c) * 2;
+            mma_16816(acc[j], a, lds32(row), lds32(row + 16));
+          }
+        }
+      }
+      const int first_c = p.whole ? cta : owner_cta(pu0, p.total, G);
+      const int last_c = p.whole ? cta : owner_cta(pu0 + p.units - 1, p.total, G);
+      if (first_c == last_c) {
+        // the whole panel is this CTA's
+#pragma unroll
+        for (int j = 0; j < MT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int tok = 8 * j + 2 * c + (e & 1), n = n0 + 16 * ew + g4 + 8 * (e >> 1);
+            if (ok && tok < p.M && n < p.N)
+              p.Y[static_cast<int64_t>(tok) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j][e]));
+          }
+      } else {
+        const int my_slot = 2 * cta + (panel == first_panel ? 0 : 1);
+        float* part = p.partials + static_cast<int64_t>(my_slot) * kPartialFloats;
+#pragma unroll
+        for (int j = 0; j < MT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            __stcg(part + (8 * j + 2 * c + (e & 1)) * kPanelRows + 16 * ew + g4 + 8 * (e >> 1), acc[j][e]);
+        __threadfence();
+        named_bar_sync(kEpiBar, kEpilogueThreads);
+        if (et == 0) {
+          if (!waited) griddep_wait();   // the counters are zeroed by the kernel before this one
+          __threadfence();
+          const int arrived = atomicAdd(p.counters + panel, 1);
+          s_last = (ok && arrived == last_c - first_c) ? 1 : 0;
+          if (s_last) __threadfence();
+        }
+        waited = true;
+        named_bar_sync(kEpiBar, kEpilogueThreads);
+        if (s_last) {
+          // the last CTA to finish a piece of this panel adds the pieces in CTA order
+#pragma unroll
+          for (int j = 0; j < MT; ++j)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tok = 8 * j + 2 * c + (e & 1), row = 16 * ew + g4 + 8 * (e >> 1);
+              float sum = 0.f;
+              for (int q = first_c; q <= last_c; ++q) {
+                const long long q_begin = p.total * q / G;
+                const int q_slot = 2 * q + (static_cast<int>(q_begin / p.units) == panel ? 0 : 1);
+                sum += __ldcg(p.partials + static_cast<int64_t>(q_slot) * kPartialFloats + tok * kPanelRows + row);
+              }
+              if (tok < p.M && n0 + row < p.N)
+                p.Y[static_cast<int64_t>(tok) * p.N + n0 + row] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+            }
+        }
+      }
+      named_bar_sync(kEpiBar, kEpilogueThreads);   // B, bf16(s*T) and s_last are reused by the next segment
+      seg = seg_end;
+    }
+    return;
+  }
+
+  // ---- consumers
   const uint8_t* const lut_b = gbase + S::kLutOffset;
   const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
   const int kw = warp % kSlices, gh = warp / kSlices;
-  const int first_panel = static_cast<int>(u_begin / p.units);
-  bool waited = false;
+  mbar_wait(bar_table, 0, ab);   // the decode table has landed
   int i = 0;   // stage index within the CTA's range
-
-  for (long long seg = u_begin; seg < u_end;) {
+  int k = 0;   // segment index
+  for (long long seg = u_begin; seg < u_end; ++k) {
     const int panel = static_cast<int>(seg / p.units);
     const long long pu0 = static_cast<long long>(panel) * p.units;
     const long long seg_end = u_end < pu0 + p.units ? u_end : pu0 + p.units;
-    const int n0 = panel * kPanelRows;
-    // the CTA holding the panel's first stage adds the low-rank term; bf16(s*T)
-    // needs the kernel before this one, so in the CTA's first segment it is
-    // fetched after the stages, where waiting for that kernel holds up nothing
-    const bool lowrank = seg == pu0;
-    const bool t_early = lowrank && seg != u_begin;
-    if (lowrank) {
-      stage_lowrank_b(p, n0, bs, t);
-      if (t_early && warp == 0) {
-        if (!waited) {
-          griddep_wait();
-          waited = true;
-        }
-        stage_lowrank_t<MT>(p, ts, lane);
-      }
-    }
 
     float acc[2][MT][4];
 #pragma unroll
@@ -362,15 +458,10 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
     }
-    if (lowrank && !t_early && warp == 0) {
-      if (!waited) {
-        griddep_wait();
-        waited = true;
-      }
-      stage_lowrank_t<MT>(p, ts, lane);
-    }
 
-    // the warp's rows of its slice's partial panel -> shared memory, [token][row]
+    // the warp's rows of its slice's partial panel -> shared memory, [token][row],
+    // once the epilogue has taken the previous segment's
+    if (k > 0) __all_sync(0xffffffffu, mbar_wait(bar_slots_free, (k - 1) & 1, ab));
     float* slot = slots + kw * kSlotFloats;
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -383,68 +474,8 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
         slot[(tok + 1) * kSlotStride + row + 8] = acc[h][j][3];
       }
     }
-    if (lowrank) {
-      cp_async_wait_all();
-      named_bar_sync(kNamedBar, kConsumers);   // every copy of B and bf16(s*T) has landed
-      if (warp < 4) {   // row group `warp`, into the partial of slice `warp` (slot == slice here)
-        __syncwarp();
-        lowrank_group<MT>(p, bs, ts, slot, warp, lane);
-      }
-    }
-    named_bar_sync(kNamedBar, kConsumers);
-
-    const int first_c = p.whole ? cta : owner_cta(pu0, p.total, G);
-    const int last_c = p.whole ? cta : owner_cta(pu0 + p.units - 1, p.total, G);
-    constexpr int kOut = kPanelRows * 8 * MT;
-    if (first_c == last_c) {
-      // the whole panel is this CTA's: sum the warps in order and store
-      for (int o = t; o < kOut; o += kConsumers) {
-        const int tok = o >> 6, row = o & 63;
-        float sum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kSlices; ++w) sum += slots[w * kSlotFloats + tok * kSlotStride + row];
-        if (tok < p.M && n0 + row < p.N)
-          p.Y[static_cast<int64_t>(tok) * p.N + n0 + row] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
-      }
-    } else {
-      const int my_slot = 2 * cta + (panel == first_panel ? 0 : 1);
-      float* part = p.partials + static_cast<int64_t>(my_slot) * kPartialFloats;
-      for (int o = t; o < kOut; o += kConsumers) {
-        const int tok = o >> 6, row = o & 63;
-        float sum = 0.f;
-#pragma unroll
-        for (int w = 0; w < kSlices; ++w) sum += slots[w * kSlotFloats + tok * kSlotStride + row];
-        __stcg(part + o, sum);
-      }
-      __threadfence();
-      named_bar_sync(kNamedBar, kConsumers);
-      if (t == 0) {
-        if (!waited) {
-          griddep_wait();   // the counters are zeroed by the kernel before this one
-          waited = true;
-        }
-        __threadfence();
-        const int arrived = atomicAdd(p.counters + panel, 1);
-        s_last = (arrived == last_c - first_c) ? 1 : 0;
-        if (s_last) __threadfence();
-      }
-      named_bar_sync(kNamedBar, kConsumers);
-      if (s_last) {
-        // the last CTA to finish a piece of this panel adds the pieces in CTA order
-        for (int o = t; o < kOut; o += kConsumers) {
-          const int tok = o >> 6, row = o & 63;
-          float sum = 0.f;
-          for (int q = first_c; q <= last_c; ++q) {
-            const long long q_begin = p.total * q / G;
-            const int q_slot = 2 * q + (static_cast<int>(q_begin / p.units) == panel ? 0 : 1);
-            sum += __ldcg(p.partials + static_cast<int64_t>(q_slot) * kPartialFloats + o);
-          }
-          if (tok < p.M && n0 + row < p.N)
-            p.Y[static_cast<int64_t>(tok) * p.N + n0 + row] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
-        }
-      }
-    }
-    named_bar_sync(kNamedBar, kConsumers);   // the slots are reused by the next segment
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar_slots_full);
     seg = seg_end;
   }
 }
@@ -485,9 +516,22 @@ bool stream_applies(const LayerDims& d, const Workspace& ws, int sms) {
   return ws.partial_bytes >= stream_partial_bytes(sms);
 }
 
+// The compile-time bf16 table against the fp32 levels, rounded to nearest even.
+bool level_table_matches() {
+  for (int i = 0; i < 16; ++i) {
+    uint32_t u;
+    std::memcpy(&u, &kNF4LevelsHost[i], sizeof(u));
+    const uint32_t r = (u + 0x7FFFu + ((u >> 16) & 1u)) >> 16;
+    if (r != kLevelBf16[i]) return false;
+  }
+  return true;
+}
+
 cudaError_t launch_stream_fwd(const LayerDims& d, const uint16_t* X, const uint8_t* packed, const float* absmax,
                               const uint16_t* B, const Workspace& ws, uint16_t* Y, int* status, int sms,
                               cudaStream_t stream) {
+  static const bool table_ok = level_table_matches();
+  if (!table_ok) return cudaErrorInvalidValue;
   const int mt = d.M <= 8 ? 1 : 2;
   CUtensorMap maps[3];
   // codes [N, K/2] bytes, 128-byte rows of 64-row boxes, swizzled; absmax [N, K/64]
