@@ -253,6 +253,24 @@ def cpu_baseline(sh, min_seconds=10.0):
                       f"{per_call * 1e3:.1f} ms per call"}
 
 
+# ---------------------------------------------------------------- multi-rank helpers
+
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The job's time: the slowest rank's (all ranks get it).  One rank: unchanged."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(work_per_rank_step: float, ms_step: float, world: int) -> float:
+    """Whole-job rate: the work every rank did per step over the (max-over-ranks) step time."""
+    return work_per_rank_step * world / (ms_step * 1e-3)
+
+
 # ---------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -352,12 +370,7 @@ def run_ours(args):
         end.record(stream)
         torch.cuda.synchronize()
         barrier()
-        ms = start.elapsed_time(end)
-        if world > 1:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        return ms
+        return max_over_ranks(start.elapsed_time(end), world, dev)
 
     for i in range(args.warmup):
         step(i)
@@ -376,8 +389,8 @@ def run_ours(args):
     ms_step = total_ms / args.steps
     flops = step_flops(sh)
     tflops_rank = flops / (ms_step * 1e-3) / 1e12
-    value = tflops_rank * world
-    tokens_per_s = M * world / (ms_step * 1e-3)
+    value = job_rate(flops, ms_step, world) / 1e12
+    tokens_per_s = job_rate(M, ms_step, world)
 
     # ---- same region again with every library launch bracketed by CUDA events
     qlora.qlora_profile_enable(True)
