@@ -176,7 +176,11 @@ size_t qlora_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int32_t r);
  *   workspace / workspace_bytes: caller scratch, >= qlora_workspace_bytes().
  * Requires M >= 0 (M == 0 launches nothing), d_in % 64 == 0, d_out % 8 == 0,
  * 1 <= r <= 128.  Accuracy: fp32 accumulation of bf16 products; the LoRA term
- * enters the tensor-core accumulator as bf16(s*T) x B.
+ * enters the tensor-core accumulator as bf16(s*T) x B.  For 1..16 tokens with
+ * d_in % 256 == 0 the weight is streamed by a separate kernel that multiplies
+ * bf16(level[q]) by X and applies each block's absmax to the block sum in fp32:
+ * the same result up to the rounding of the weight (both within 2^-9 of
+ * level[q] * absmax).
  */
 qlora_status qlora_linear_fwd(const uint16_t* X, int64_t M, int64_t d_in, int64_t d_out,
                               const uint8_t* packed, const float* absmax,
