@@ -37,8 +37,10 @@ def _noalloc_call(lib, X, packed, absmax, A, B, s, Y, XA):
 
 
 @pytest.mark.parametrize("case", [(300, 320, 136, 12, 1.5),      # r % 8 != 0: padded A in the array
-                                  (4096, 4096, 4096, 16, 1.0)],   # the q_proj projection
-                         ids=["ragged_r12", "q_proj"])
+                                  (4096, 4096, 4096, 16, 1.0),    # the q_proj projection
+                                  (16, 4096, 4096, 16, 1.0)],     # 16 tokens: panels shared by CTAs, their
+                                                                  # counters and partials in the array
+                         ids=["ragged_r12", "q_proj", "tokens16_split_panels"])
 def test_noalloc_forward_matches_workspace_forward_twice(case):
     from rank_adapter_linear_nf4_b300 import qlora
     M, K, N, r, s = case
