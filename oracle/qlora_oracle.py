@@ -270,30 +270,36 @@ def swiglu_backward(gu, dh) -> np.ndarray:
     return np.concatenate([dh * u * sg * (1.0 + g * (1.0 - sg)), dh * g * sg], axis=1)
 
 
-def swiglu_mlp_forward(X, Wd_gu, A_gu, B_gu, Wd_d, A_d, B_d, s: float):
+def _stored(x, store_bf16: bool):
+    return bf16_round(x) if store_bf16 else _f64(x)
+
+
+def swiglu_mlp_forward(X, Wd_gu, A_gu, B_gu, Wd_d, A_d, B_d, s: float, store_bf16: bool = True):
     """The SwiGLU MLP block of two LoRA layers: Y = down(swiglu(gate_up(X))).
 
     gate_up is one layer whose output columns are [gate | up] (the stacked
-    projection); its output and h are stored as bf16 between the layers, as the
-    block keeps them, and are rounded to bf16 here.  Returns Y and the saved
-    tensors (gu, T_gu, h, T_d).
+    projection).  With ``store_bf16`` its output and h are rounded to bf16
+    between the layers, as the block stores them; without it they stay fp64
+    (the exact composition, which the finite-difference pin uses).  Returns Y
+    and the saved tensors (gu, T_gu, h, T_d).
     """
     gu, T_gu = lora_forward(X, Wd_gu, A_gu, B_gu, s)
-    gu = bf16_round(gu)
-    h = bf16_round(swiglu_forward(gu))
+    gu = _stored(gu, store_bf16)
+    h = _stored(swiglu_forward(gu), store_bf16)
     Y, T_d = lora_forward(h, Wd_d, A_d, B_d, s)
     return Y, (gu, T_gu, h, T_d)
 
 
-def swiglu_mlp_backward(X, dY, saved, Wd_gu, A_gu, B_gu, Wd_d, A_d, B_d, s: float):
+def swiglu_mlp_backward(X, dY, saved, Wd_gu, A_gu, B_gu, Wd_d, A_d, B_d, s: float, store_bf16: bool = True):
     """Gradients of the block: dX, (dA_gu, dB_gu), (dA_d, dB_d).
 
-    dh comes out of the down layer's backward and dgu out of the gate's, both
-    stored as bf16 between the steps (rounded here), as the block keeps them.
+    dh comes out of the down layer's backward and dgu out of the gate's; with
+    ``store_bf16`` both are rounded to bf16 between the steps, as the block
+    stores them, otherwise they stay fp64.
     """
     gu, T_gu, h, T_d = saved
     dh, dA_d, dB_d = lora_backward(h, dY, Wd_d, A_d, B_d, s, T=T_d)
-    dh = bf16_round(dh)
-    dgu = bf16_round(swiglu_backward(gu, dh))
+    dh = _stored(dh, store_bf16)
+    dgu = _stored(swiglu_backward(gu, dh), store_bf16)
     dX, dA_gu, dB_gu = lora_backward(X, dgu, Wd_gu, A_gu, B_gu, s, T=T_gu)
     return dX, (dA_gu, dB_gu), (dA_d, dB_d)

@@ -375,3 +375,58 @@ def test_swiglu_backward_matches_finite_differences():
         m[idx] -= eps
         num[idx] = np.sum((O.swiglu_forward(p) - O.swiglu_forward(m)) * dh) / (2 * eps)
     np.testing.assert_allclose(grad, num, rtol=1e-7, atol=1e-9)
+
+
+def test_swiglu_mlp_block_backward_matches_finite_differences():
+    """The whole block (gate/up layer, gate, down layer) with fp64 intermediates:
+    the gradients of L = <Y, R> by central differences in X, A and B of both layers."""
+    rng = np.random.default_rng(9)
+    M, dm, dff, r, s = 3, 8, 6, 2, 0.7
+    X = rng.normal(size=(M, dm))
+    Wgu = rng.normal(size=(2 * dff, dm)) * 0.5
+    Wd = rng.normal(size=(dm, dff)) * 0.5
+    Agu, Bgu = rng.normal(size=(dm, r)), rng.normal(size=(r, 2 * dff))
+    Ad, Bd = rng.normal(size=(dff, r)), rng.normal(size=(r, dm))
+    R = rng.normal(size=(M, dm))
+
+    def loss(X_, Agu_, Bgu_, Ad_, Bd_):
+        Y, _ = O.swiglu_mlp_forward(X_, Wgu, Agu_, Bgu_, Wd, Ad_, Bd_, s, store_bf16=False)
+        return float(np.sum(Y * R))
+
+    Y, saved = O.swiglu_mlp_forward(X, Wgu, Agu, Bgu, Wd, Ad, Bd, s, store_bf16=False)
+    dX, (dAgu, dBgu), (dAd, dBd) = O.swiglu_mlp_backward(X, R, saved, Wgu, Agu, Bgu, Wd, Ad, Bd, s,
+                                                         store_bf16=False)
+    args = [X, Agu, Bgu, Ad, Bd]
+    for k, grad in enumerate([dX, dAgu, dBgu, dAd, dBd]):
+        num = np.zeros_like(args[k])
+        for idx in np.ndindex(args[k].shape):
+            p = [a.copy() for a in args]
+            m = [a.copy() for a in args]
+            p[k][idx] += 1e-6
+            m[k][idx] -= 1e-6
+            num[idx] = (loss(*p) - loss(*m)) / 2e-6
+        # central-difference noise is ~1e-7 here; a wrong term or sign is off by O(1)
+        np.testing.assert_allclose(grad, num, rtol=1e-5, atol=1e-7)
+
+
+def test_swiglu_mlp_block_forward_one_hot():
+    """One-hot token and exact NF4 weights (entries in {-a, 0, a}, one at +-a per
+    block): Y picks one column of the down weight times silu(g) * u of one
+    feature, with g, u read off the stacked weight; silu by scipy's expit."""
+    from scipy.special import expit
+    dm, dff, k = 64, 8, 5
+    Wgu = np.zeros((2 * dff, dm), dtype=np.float32)
+    Wgu[3, k], Wgu[dff + 3, k] = 0.5, -0.25            # g_3 = 0.5, u_3 = -0.25; every other feature 0
+    Wd = np.zeros((dm, dff), dtype=np.float32)
+    Wd[7, 3] = 2.0                                     # Y[:, 7] = 2 h_3
+    for W in (Wgu, Wd):
+        q, a = O.quantize_nf4(W)
+        assert np.array_equal(O.dequantize_nf4(q, a, *W.shape), W)   # exact NF4 points
+    X = np.zeros((1, dm), dtype=np.float32)
+    X[0, k] = 1.0
+    Z = np.zeros
+    Y, _ = O.swiglu_mlp_forward(X, Wgu, Z((dm, 1)), Z((1, 2 * dff)), Wd, Z((dff, 1)), Z((1, dm)), 1.0,
+                                store_bf16=False)
+    want = np.zeros((1, dm))
+    want[0, 7] = 2.0 * 0.5 * expit(0.5) * -0.25
+    np.testing.assert_allclose(Y, want, rtol=1e-14, atol=1e-300)
