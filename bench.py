@@ -6,6 +6,12 @@ of the projection workload over one batch of synthetic tokens, inputs already
 resident in HBM.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+                  [--no-extra] [--no-cpu-baseline]
+
+The default workload is the largest single-GPU one: 16384 tokens through a
+4096 -> 14336 projection at rank 64 (the top of the token sweep).  Besides the
+headline line the same run measures the other projection workloads (key
+"extra") with shorter timed regions.
 
 N > 1 is launched by torchrun: each rank runs its own independent replica of
 the workload on its own GPU (no collective on the data path; "scaling": "weak").
@@ -14,6 +20,7 @@ the workload on its own GPU (no collective on the data path; "scaling": "weak").
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -27,7 +34,13 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "fused QLoRA linear fwd+bwd TFLOP/s & tokens/s; % of BF16 TC / HBM roofline"
-DEFAULT_CONFIG = "llama3_8b_q_proj"
+DEFAULT_CONFIG = "sweep_m16384"
+# Workloads measured beside the headline one (shorter timed regions each).
+EXTRA_CONFIGS = ("llama3_8b_q_proj", "llama3_8b_mlp_up", "llama3_8b_mlp_down", "qwen14b_attn", "qwen14b_mlp",
+                 "sweep_m1", "sweep_m16", "sweep_m128", "sweep_m1024")
+# A timed region shorter than this runs at burst clocks: its roofline takes the
+# burst bf16 peak; longer regions take the sustained (power-capped) one.
+BURST_REGION_S = 1.0
 
 
 def shape_of(name):
@@ -47,6 +60,19 @@ def step_flops(sh) -> float:
     fwd = 2 * M * K * N + 2 * M * r * (K + N)
     bwd = 2 * M * K * N + 4 * M * r * (K + N)
     return float(fwd if fwd_only(sh) else fwd + bwd)
+
+
+def step_bytes(sh) -> float:
+    """Algorithmic HBM bytes of one step: the NF4 weight (codes + fp32 absmax)
+    once per pass, the bf16 activations read and written, the low-rank factors
+    and the small fp32 outputs."""
+    M, K, N, r = sh.M, sh.d_in, sh.d_out, sh.r
+    w = 0.5625 * K * N
+    fwd = w + 2.0 * M * K + 2.0 * M * N + 2.0 * r * (K + N) + 4.0 * M * r
+    if fwd_only(sh):
+        return fwd
+    bwd = w + 2.0 * M * N * 2 + 2.0 * M * K * 2 + 2.0 * r * (K + N) + 4.0 * M * r + 4.0 * r * (K + N)
+    return fwd + bwd
 
 
 def sources_hash() -> str:
@@ -75,12 +101,23 @@ def stored_traffic(kernel: str, workload: str):
 
 
 def kernel_work(sh, kind):
-    """Algorithmic (flops, bytes) of one launch of a main fused kernel."""
+    """Algorithmic (flops, bytes) of one launch of a kernel of the layer."""
     M, K, N, r = sh.M, sh.d_in, sh.d_out, sh.r
     w_bytes = 0.5625 * K * N
     if kind == "lora_main_fwd":
         return 2.0 * M * K * N + 2.0 * M * r * N, w_bytes + 2.0 * M * K + 2.0 * M * N + 2.0 * M * r + 2.0 * r * N
-    return 2.0 * M * K * N + 2.0 * M * r * K, w_bytes + 2.0 * M * N + 2.0 * M * K + 2.0 * M * r + 2.0 * r * K
+    if kind == "lora_main_dX":
+        return 2.0 * M * K * N + 2.0 * M * r * K, w_bytes + 2.0 * M * N + 2.0 * M * K + 2.0 * M * r + 2.0 * r * K
+    if kind == "lora_stream_fwd":
+        return (2.0 * M * K * N + 2.0 * M * r * N,
+                w_bytes + 2.0 * M * K + 2.0 * M * N + 2.0 * r * N + 2.0 * M * r)
+    if kind == "lora_rows_T":
+        return 2.0 * M * K * r, 2.0 * M * K + 2.0 * K * r + 6.0 * M * r
+    if kind == "lora_rows_G":
+        return 2.0 * M * N * r, 2.0 * M * N + 2.0 * N * r + 8.0 * M * r
+    if kind == "lora_red_dA_dB":
+        return 2.0 * M * r * (K + N), 2.0 * M * (K + N) + 4.0 * M * r + 4.0 * r * (K + N)
+    return 0.0, 0.0
 
 
 def workload_desc(sh) -> str:
@@ -99,101 +136,142 @@ def load_peaks():
     return {"hbm": 6400.0, "bf16": 1800.0, "bf16_sust": 1400.0, "src": "fallback"}
 
 
+def tensor_peak(peaks, region_s):
+    """The bf16 peak a region of this length is judged against, and its name."""
+    if region_s < BURST_REGION_S:
+        return peaks["bf16"], f"bf16 dense burst ({peaks['src']}; timed region {region_s * 1e3:.0f} ms < 1 s)"
+    return peaks["bf16_sust"], f"bf16 dense sustained ({peaks['src']}; timed region {region_s:.1f} s)"
+
+
 # ---------------------------------------------------------------- clocks (NVML)
 
+class _Nvml:
+    """The few read-only NVML queries the sampler needs, through pynvml when it
+    is importable, else straight from the driver's libnvidia-ml with ctypes."""
+
+    CLOCK_SM = 1
+
+    def __init__(self, torch_dev: int):
+        import torch
+        uuid = str(torch.cuda.get_device_properties(torch_dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.py = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            self.source = "pynvml"
+            return
+        except Exception:
+            self.py = None
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit_v2 failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByUUID failed")
+        self.source = "libnvidia-ml (ctypes)"
+        fn = None
+        for name in ("nvmlDeviceGetCurrentClocksEventReasons", "nvmlDeviceGetCurrentClocksThrottleReasons"):
+            if hasattr(lib, name):
+                fn = getattr(lib, name)
+                break
+        self._reasons_fn = fn
+
+    def sm_mhz(self) -> int:
+        if self.py:
+            return int(self.py.nvmlDeviceGetClockInfo(self.h, self.py.NVML_CLOCK_SM))
+        v = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, ctypes.byref(v)) != 0:
+            raise RuntimeError("nvmlDeviceGetClockInfo")
+        return int(v.value)
+
+    def max_sm_mhz(self) -> int:
+        if self.py:
+            return int(self.py.nvmlDeviceGetMaxClockInfo(self.h, self.py.NVML_CLOCK_SM))
+        v = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, ctypes.byref(v)) != 0:
+            raise RuntimeError("nvmlDeviceGetMaxClockInfo")
+        return int(v.value)
+
+    def power_w(self) -> float:
+        if self.py:
+            return self.py.nvmlDeviceGetPowerUsage(self.h) / 1000.0
+        v = ctypes.c_uint()
+        if self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(v)) != 0:
+            raise RuntimeError("nvmlDeviceGetPowerUsage")
+        return v.value / 1000.0
+
+    def reasons(self) -> int:
+        if self.py:
+            for fn in ("nvmlDeviceGetCurrentClocksEventReasons", "nvmlDeviceGetCurrentClocksThrottleReasons"):
+                if hasattr(self.py, fn):
+                    return int(getattr(self.py, fn)(self.h))
+            return 0
+        if self._reasons_fn is None:
+            return 0
+        v = ctypes.c_ulonglong()
+        if self._reasons_fn(self.h, ctypes.byref(v)) != 0:
+            return 0
+        return int(v.value)
+
+
 class ClockSampler:
-    """Samples SM clock, power and clock-event reasons during the timed region:
-    NVML every ~10 ms in a thread, else `nvidia-smi -lms 100` in the background."""
+    """Samples the SM clock, power and clock-event reasons every ~2 ms in a
+    thread from before the warm-up to the end of the run; each timed region
+    keeps the samples taken inside it (host time stamps)."""
 
     REASONS = [("gpu_idle", 0x1), ("applications_clocks", 0x2), ("sw_power_cap", 0x4),
                ("hw_slowdown", 0x8), ("sync_boost", 0x10), ("sw_thermal_slowdown", 0x20),
                ("hw_thermal_slowdown", 0x40), ("hw_power_brake", 0x80)]
-    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active"]
 
-    def __init__(self, torch_dev: int):
-        self.mode = None
+    def __init__(self, torch_dev: int, period_s: float = 0.002):
         self.samples = []
         self.err = ""
+        self.period = period_s
+        self.nv = None
         try:
-            import pynvml
-            import torch
-            pynvml.nvmlInit()
-            self.nv = pynvml
-            try:
-                uuid = str(torch.cuda.get_device_properties(torch_dev).uuid)
-                self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid if uuid.startswith("GPU-") else "GPU-" + uuid)
-            except Exception:
-                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-                idx = int(vis.split(",")[torch_dev]) if vis and vis.split(",")[0].isdigit() else torch_dev
-                self.h = pynvml.nvmlDeviceGetHandleByIndex(idx)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.mode = "nvml"
+            self.nv = _Nvml(torch_dev)
+            self.max_mhz = self.nv.max_sm_mhz()
         except Exception as e:
-            self.err = f"NVML: {e!r}"
-            import shutil
-            if shutil.which("nvidia-smi"):
-                self.mode = "smi"
-                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-                self.smi_index = vis.split(",")[torch_dev] if vis else str(torch_dev)
-
-    def _reasons(self):
-        nv = self.nv
-        for fn in ("nvmlDeviceGetCurrentClocksEventReasons", "nvmlDeviceGetCurrentClocksThrottleReasons"):
-            if hasattr(nv, fn):
-                return int(getattr(nv, fn)(self.h))
-        return 0
+            self.err = f"NVML unavailable: {e!r}"[:200]
+            self.max_mhz = None
 
     def _run(self):
         while not self._stop.is_set():
             try:
-                sm = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
-                pw = self.nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
-                self.samples.append((sm, pw, self._reasons()))
+                self.samples.append((time.perf_counter(), self.nv.sm_mhz(), self.nv.power_w(), self.nv.reasons()))
             except Exception:
                 pass
-            time.sleep(0.01)
+            time.sleep(self.period)
 
     def start(self):
-        if self.mode == "nvml":
-            self._stop = threading.Event()
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
-        elif self.mode == "smi":
-            import subprocess
-            self._p = subprocess.Popen(
-                ["nvidia-smi", "-i", self.smi_index, "--query-gpu=" + ",".join(self.SMI_FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        if self.nv is None:
+            return
+        self._stop = threading.Event()
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
 
     def stop(self):
-        if self.mode == "nvml":
+        if self.nv is not None:
             self._stop.set()
             self._t.join()
-        elif self.mode == "smi":
-            self._p.terminate()
-            out, _ = self._p.communicate(timeout=10)
-            self.max_mhz = None
-            for line in out.strip().splitlines():
-                f = [x.strip() for x in line.split(",")]
-                try:
-                    self.max_mhz = float(f[1])
-                    self.samples.append((float(f[0]), float(f[2]), int(f[3], 16)))
-                except (ValueError, IndexError):
-                    pass
-        else:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "no clock source: " + self.err}
-        s = self.samples
+
+    def summary(self, t0: float, t1: float):
+        """Clocks seen in the host-time window [t0, t1]."""
+        if self.nv is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": self.err}
+        s = [x for x in self.samples if t0 <= x[0] <= t1]
         mask = 0
-        for _, _, r in s:
-            mask |= r
+        for x in s:
+            mask |= x[3]
         reasons = [n for n, b in self.REASONS if mask & b and n != "gpu_idle"]
-        out = {"sm_mhz": statistics.median([x[0] for x in s]) if s else None,
+        out = {"sm_mhz": statistics.median([x[1] for x in s]) if s else None,
+               "sm_min_mhz": min(x[1] for x in s) if s else None,
                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(s),
-               "power_w_median": statistics.median([x[1] for x in s]) if s else None,
-               "source": self.mode}
-        if self.err:
-            out["note"] = self.err
+               "power_w_median": statistics.median([x[2] for x in s]) if s else None,
+               "window_ms": (t1 - t0) * 1e3, "period_ms": self.period * 1e3, "source": self.nv.source}
         return out
 
 
@@ -212,17 +290,22 @@ class OracleRunner:
         f = lambda t: t.float().numpy()
         self.X, self.dY, self.A, self.B = f(X), f(dY), f(A), f(B)
         self.packed, self.absmax = O.quantize_nf4(f(W))
+        self.fwd_only = fwd_only(sh)
+
+    @staticmethod
+    def blas_threads() -> int:
         try:
             from threadpoolctl import threadpool_info
-            self.threads = max([int(i.get("num_threads", 1)) for i in threadpool_info()] or [1])
+            return max([int(i.get("num_threads", 1)) for i in threadpool_info()] or [1])
         except Exception:
-            self.threads = os.cpu_count() or 1
+            return os.cpu_count() or 1
 
     def step(self):
         O, sh = self.O, self.sh
         Wd = O.dequantize_nf4(self.packed, self.absmax, sh.d_out, sh.d_in)
         _, T = O.lora_forward(self.X, Wd, self.A, self.B, sh.s)
-        O.lora_backward(self.X, self.dY, Wd, self.A, self.B, sh.s, T=T)
+        if not self.fwd_only:
+            O.lora_backward(self.X, self.dY, Wd, self.A, self.B, sh.s, T=T)
 
     def time_calls(self, min_seconds: float, max_calls: int = 1000):
         times = []
@@ -242,15 +325,31 @@ def sample_shape(sh, tokens):
 
 
 def cpu_baseline(sh, min_seconds=10.0):
+    """The oracle on the host cores, all BLAS threads, then one thread, each on a
+    bounded sample of the workload's tokens (the full weight every step)."""
     tokens = min(sh.M, 256)
     runner = OracleRunner(sh, tokens)
+    threads = runner.blas_threads()
     per_call, calls = runner.time_calls(min_seconds)
     flops = step_flops(sample_shape(sh, tokens))
-    return {"value": flops / per_call / 1e12, "unit": "TFLOP/s", "cores": runner.threads, "kind": "oracle",
-            "tokens_per_s": tokens / per_call,
-            "sample": f"{tokens} of {sh.M} tokens of the same workload (NF4 dequantise of the full "
-                      f"weight + fp64 forward + backward), median of {calls} calls, "
-                      f"{per_call * 1e3:.1f} ms per call"}
+    out = {"value": flops / per_call / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "tokens_per_s": tokens / per_call,
+           "sample": f"{tokens} of {sh.M} tokens of the same workload (NF4 dequantise of the full "
+                     f"weight + fp64 forward{'' if fwd_only(sh) else ' + backward'}), median of {calls} calls, "
+                     f"{per_call * 1e3:.1f} ms per call, {threads} BLAS threads"}
+    try:
+        from threadpoolctl import threadpool_limits
+        t1 = min(sh.M, 32)
+        r1 = OracleRunner(sh, t1)
+        with threadpool_limits(limits=1):
+            pc1, c1 = r1.time_calls(min_seconds / 2)
+        f1 = step_flops(sample_shape(sh, t1))
+        out["single_thread"] = {"value": f1 / pc1 / 1e12, "unit": "TFLOP/s", "cores": 1,
+                                "tokens_per_s": t1 / pc1,
+                                "sample": f"{t1} tokens, median of {c1} calls, {pc1 * 1e3:.1f} ms per call"}
+    except Exception as e:   # report, do not fail the run
+        out["single_thread"] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    return out
 
 
 # ---------------------------------------------------------------- multi-rank helpers
@@ -280,7 +379,7 @@ def run_reference(args):
     sh = shape_of(args.config)
     tokens = min(sh.M, 128)
     runner = OracleRunner(sh, tokens)
-    threads = runner.threads
+    threads = runner.blas_threads()
     for _ in range(args.warmup):
         runner.step()
     t0 = time.perf_counter()
@@ -298,7 +397,8 @@ def run_reference(args):
         "config": {"workload": workload_desc(sh), "sample_tokens_per_step": tokens},
         "tokens_per_s": tokens / per_step,
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-                         "sample": f"each step: {tokens} of {sh.M} tokens (dequantise + fp64 fwd + bwd)"},
+                         "sample": f"each step: {tokens} of {sh.M} tokens (dequantise + fp64 fwd"
+                                   f"{'' if fwd_only(sh) else ' + bwd'})"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -307,10 +407,157 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU arm
 
+class Workload:
+    """Resident inputs of one workload on the device, rotated over enough
+    copies that no step finds its inputs in L2 (the copies sit at different
+    addresses; L2 is physically indexed, so a copy is as cold as new data)."""
+
+    def __init__(self, sh, dev, rank: int, l2: int):
+        import torch
+        from rank_adapter_linear_nf4_b300 import qlora, synthetic
+        self.sh = sh
+        M, K, N, r = sh.M, sh.d_in, sh.d_out, sh.r
+        self.only_fwd = fwd_only(sh)
+        read = 2 * M * K + 0.5625 * K * N + (0 if self.only_fwd else 2 * M * N)
+        written = 2 * M * N + (0 if self.only_fwd else 2 * M * K)
+        self.set_bytes = read + written
+        self.n_sets = max(2, math.ceil(2.0 * l2 / self.set_bytes))
+        self.l2 = l2
+        self.ws = torch.empty(max(16, qlora.qlora_workspace_bytes(M, K, N, r)), dtype=torch.uint8, device=dev)
+        inp = synthetic.layer_inputs(sh, seed=2 + 2 * rank)
+        X, dY, W, A, B = (inp[k].to(dev) for k in ("X", "dY", "W", "A", "B"))
+        packed, absmax = qlora.qlora_quantize_nf4(W)
+        del W
+        self.sets = []
+        for i in range(self.n_sets):
+            c = (lambda t: t) if i == 0 else (lambda t: t.clone())
+            self.sets.append(dict(X=c(X), dY=None if self.only_fwd else c(dY), packed=c(packed),
+                                  absmax=c(absmax), A=c(A), B=c(B),
+                                  Y=torch.empty(M, N, dtype=torch.bfloat16, device=dev),
+                                  XA=torch.empty(M, r, dtype=torch.float32, device=dev),
+                                  dX=None if self.only_fwd else torch.empty(M, K, dtype=torch.bfloat16, device=dev),
+                                  dA=torch.empty(K, r, dtype=torch.float32, device=dev),
+                                  dB=torch.empty(r, N, dtype=torch.float32, device=dev)))
+        self.dY0 = dY
+        torch.cuda.synchronize()
+
+    def step(self, i):
+        from rank_adapter_linear_nf4_b300 import qlora
+        sh, t = self.sh, self.sets[i % self.n_sets]
+        qlora.qlora_linear_fwd(t["X"], t["packed"], t["absmax"], t["A"], t["B"], sh.s,
+                               Y=t["Y"], XA=t["XA"], workspace=self.ws)
+        if not self.only_fwd:
+            qlora.qlora_linear_bwd(t["X"], t["dY"], t["packed"], t["absmax"], t["A"], t["B"], sh.s,
+                                   t["XA"], dX=t["dX"], dA=t["dA"], dB=t["dB"], workspace=self.ws)
+
+    def l2_note(self):
+        return (f"inputs rotated over {self.n_sets} resident copies of {self.set_bytes / 1e6:.0f} MB "
+                f"(> 2x the {self.l2 / 1e6:.0f} MB L2)")
+
+
+def make_timer(stream, world, dev, barrier):
+    import torch
+
+    def timed(fn, steps):
+        """(max-over-ranks ms, host start, host end) of `steps` calls of fn."""
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier()
+        h0 = time.perf_counter()
+        start.record(stream)
+        for i in range(steps):
+            fn(i)
+        end.record(stream)
+        torch.cuda.synchronize()
+        h1 = time.perf_counter()
+        barrier()
+        return max_over_ranks(start.elapsed_time(end), world, dev), h0, h1
+    return timed
+
+
+def per_kernel_profile(wl, steps, timed):
+    """The same steps with every library launch bracketed by CUDA events on its
+    stream: per kind, launches, total ms, average us, share."""
+    from rank_adapter_linear_nf4_b300 import qlora
+    qlora.qlora_profile_enable(True)
+    qlora.qlora_profile_collect()
+    prof_ms, _, _ = timed(wl.step, steps)
+    kernels = qlora.qlora_profile_collect()
+    qlora.qlora_profile_enable(False)
+    total = sum(v[0] for v in kernels.values())
+    per = {k: {"launches": n, "total_ms": round(t, 4), "avg_us": round(t / n * 1e3, 2),
+               "share": round(t / total, 4)}
+           for k, (t, n) in sorted(kernels.items(), key=lambda kv: -kv[1][0])}
+    return per, prof_ms / steps
+
+
+def kernel_roofline(sh, name, avg_us, peaks, region_s):
+    """Achieved rate of one launch of `name` against its roofline (tensor for
+    the main GEMMs of large-token workloads, HBM otherwise)."""
+    kf, kb = kernel_work(sh, name)
+    t = avg_us * 1e-6
+    tpk, tkind = tensor_peak(peaks, region_s)
+    ridge = tpk * 1e12 / (peaks["hbm"] * 1e9)
+    tensor = {"achieved": kf / t / 1e12, "unit": "TFLOP/s", "peak": tpk, "frac": kf / t / 1e12 / tpk,
+              "peak_kind": tkind, "frac_of_sustained": kf / t / 1e12 / peaks["bf16_sust"],
+              "frac_of_burst": kf / t / 1e12 / peaks["bf16"]}
+    hbm = {"achieved": kb / t / 1e9, "unit": "GB/s", "peak": peaks["hbm"], "frac": kb / t / 1e9 / peaks["hbm"],
+           "peak_kind": f"HBM copy ({peaks['src']})"}
+    bound = "tensor" if kb > 0 and kf / kb >= ridge else "hbm"
+    main = tensor if bound == "tensor" else hbm
+    out = {"bound": bound, "achieved": main["achieved"], "peak": main["peak"], "unit": main["unit"],
+           "frac": main["frac"], "kernel": name, "peak_kind": main["peak_kind"],
+           "flops_per_launch": kf, "algorithmic_bytes_per_launch": kb, "avg_launch_us": avg_us,
+           "arithmetic_intensity": kf / kb if kb else None}
+    if bound == "tensor":
+        out["frac_of_sustained"] = tensor["frac_of_sustained"]
+        out["frac_of_burst"] = tensor["frac_of_burst"]
+        out["hbm_frac"] = hbm["frac"]
+    else:
+        out["tensor_frac"] = tensor["frac"]
+    return out
+
+
+def dominant_layer_kernel(kernels):
+    """The layer's heaviest GEMM-type kernel (main fused kernels, or the token-stream forward)."""
+    for k in kernels:   # sorted by total time
+        if k in ("lora_main_fwd", "lora_main_dX", "lora_stream_fwd"):
+            return k
+    return next(iter(kernels))
+
+
+def measure_extra(sh, dev, rank, l2, peaks, timed, sampler, target_s=0.15, warmup=5):
+    """One workload beside the headline: step time, per-kernel profile, rooflines."""
+    import torch
+    wl = Workload(sh, dev, rank, l2)
+    for i in range(warmup):
+        wl.step(i)
+    est_ms, _, _ = timed(wl.step, 3)
+    steps = int(max(10, min(2000, target_s / (est_ms / 3 * 1e-3))))
+    total_ms, h0, h1 = timed(wl.step, steps)
+    ms = total_ms / steps
+    kernels, prof_ms = per_kernel_profile(wl, steps, timed)
+    flops, nbytes = step_flops(sh), step_bytes(sh)
+    region_s = total_ms * 1e-3
+    tpk, tkind = tensor_peak(peaks, region_s)
+    dom = dominant_layer_kernel(kernels)
+    res = {"workload": workload_desc(sh), "steps": steps, "ms_per_step": ms,
+           "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "tokens_per_s": sh.M / (ms * 1e-3),
+           "step_frac_of_bf16": flops / (ms * 1e-3) / 1e12 / tpk, "step_peak_kind": tkind,
+           "step_hbm_gbs": nbytes / (ms * 1e-3) / 1e9, "step_frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
+           "dominant": kernel_roofline(sh, dom, kernels[dom]["avg_us"], peaks, region_s),
+           "kernels": kernels, "profiled_ms_per_step": prof_ms, "clocks": sampler.summary(h0, h1),
+           "l2": wl.l2_note()}
+    del wl
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
-    from rank_adapter_linear_nf4_b300 import qlora, synthetic
+    from rank_adapter_linear_nf4_b300 import qlora
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -329,166 +576,97 @@ def run_ours(args):
     peaks = load_peaks()
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     stream = torch.cuda.current_stream(dev)
+    timed = make_timer(stream, world, dev, barrier)
 
-    # ---- resident input sets, rotated so that no step finds its inputs in L2
-    M, K, N, r = sh.M, sh.d_in, sh.d_out, sh.r
-    set_bytes = 2 * M * K + 2 * M * N + 0.5625 * K * N + 2 * M * K + 2 * M * N
-    n_sets = max(2, math.ceil(2.0 * l2 / set_bytes))
-    sets = []
-    ws = torch.empty(max(16, qlora.qlora_workspace_bytes(M, K, N, r)), dtype=torch.uint8, device=dev)
-    for i in range(n_sets):
-        inp = synthetic.layer_inputs(sh, seed=2 * i + 2 * rank * n_sets)
-        X, dY, W, A, B = (inp[k].to(dev) for k in ("X", "dY", "W", "A", "B"))
-        packed, absmax = qlora.qlora_quantize_nf4(W)
-        del W
-        sets.append(dict(X=X, dY=dY, packed=packed, absmax=absmax, A=A, B=B,
-                         Y=torch.empty(M, N, dtype=torch.bfloat16, device=dev),
-                         XA=torch.empty(M, r, dtype=torch.float32, device=dev),
-                         dX=torch.empty(M, K, dtype=torch.bfloat16, device=dev),
-                         dA=torch.empty(K, r, dtype=torch.float32, device=dev),
-                         dB=torch.empty(r, N, dtype=torch.float32, device=dev)))
-    torch.cuda.synchronize()
-
-    only_fwd = fwd_only(sh)
-
-    def step(i):
-        t = sets[i % n_sets]
-        qlora.qlora_linear_fwd(t["X"], t["packed"], t["absmax"], t["A"], t["B"], sh.s,
-                               Y=t["Y"], XA=t["XA"], workspace=ws)
-        if not only_fwd:
-            qlora.qlora_linear_bwd(t["X"], t["dY"], t["packed"], t["absmax"], t["A"], t["B"], sh.s,
-                                   t["XA"], dX=t["dX"], dA=t["dA"], dB=t["dB"], workspace=ws)
-
-    def timed(fn, steps):
-        start = torch.cuda.Event(enable_timing=True)
-        end = torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        barrier()
-        start.record(stream)
-        for i in range(steps):
-            fn(i)
-        end.record(stream)
-        torch.cuda.synchronize()
-        barrier()
-        return max_over_ranks(start.elapsed_time(end), world, dev)
+    sampler = ClockSampler(local)
+    sampler.start()
+    wl = Workload(sh, dev, rank, l2)
 
     for i in range(args.warmup):
-        step(i)
+        wl.step(i)
     torch.cuda.synchronize()
 
     # ---- official timed region
-    sampler = ClockSampler(local)
     launches0 = qlora.qlora_launch_count()
-    sampler.start()
-    total_ms = timed(step, args.steps)
-    clocks = sampler.stop()
+    total_ms, h0, h1 = timed(wl.step, args.steps)
+    clocks = sampler.summary(h0, h1)
     launches = qlora.qlora_launch_count() - launches0
     if qlora.qlora_device_status(clear=True) != 0:
         raise RuntimeError("device status word reports an error during the timed region")
 
     ms_step = total_ms / args.steps
+    region_s = total_ms * 1e-3
     flops = step_flops(sh)
     tflops_rank = flops / (ms_step * 1e-3) / 1e12
     value = job_rate(flops, ms_step, world) / 1e12
-    tokens_per_s = job_rate(M, ms_step, world)
+    tokens_per_s = job_rate(sh.M, ms_step, world)
+
+    if args.only_steps:   # for profilers: the warm-up and the timed steps, nothing else
+        sampler.stop()
+        if rank == 0:
+            print(json.dumps({"workload": workload_desc(sh), "ms_per_step": ms_step, "value": value,
+                              "unit": "TFLOP/s", "steps": args.steps, "note": "--only-steps"}))
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
 
     # ---- same region again with every library launch bracketed by CUDA events
-    qlora.qlora_profile_enable(True)
-    qlora.qlora_profile_collect()
-    prof_total_ms = timed(step, args.steps)
-    kernels = qlora.qlora_profile_collect()
-    qlora.qlora_profile_enable(False)
-    dom = max(kernels.items(), key=lambda kv: kv[1][0])[0]
-    main_kinds = [k for k in ("lora_main_fwd", "lora_main_dX") if k in kernels]
-    roof_kind = dom if dom in ("lora_main_fwd", "lora_main_dX") else (main_kinds[0] if main_kinds else dom)
-    k_ms, k_n = kernels[roof_kind]
-    k_avg_s = k_ms / k_n * 1e-3
-    kf, kb = kernel_work(sh, roof_kind)
-    ridge = peaks["bf16_sust"] * 1e12 / (peaks["hbm"] * 1e9)
-    if kf / kb >= ridge:
-        achieved = kf / k_avg_s / 1e12
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_sust"], "unit": "TFLOP/s",
-                    "frac": achieved / peaks["bf16_sust"], "traffic": None,
-                    "kernel": roof_kind, "peak_kind": f"bf16 dense sustained ({peaks['src']})",
-                    "frac_of_burst_peak": achieved / peaks["bf16"]}
-    else:
-        achieved = kb / k_avg_s / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm"], "unit": "GB/s",
-                    "frac": achieved / peaks["hbm"], "traffic": None, "kernel": roof_kind,
-                    "peak_kind": f"HBM copy ({peaks['src']})"}
-    roofline["flops_per_launch"] = kf
-    roofline["algorithmic_bytes_per_launch"] = kb
-    roofline["avg_launch_us"] = k_avg_s * 1e6
+    per_kernel, prof_ms = per_kernel_profile(wl, args.steps, timed)
+    roof_kind = dominant_layer_kernel(per_kernel)
+    roofline = kernel_roofline(sh, roof_kind, per_kernel[roof_kind]["avg_us"], peaks, region_s)
     roofline["traffic"] = stored_traffic(roof_kind, sh.name)
     roofline["traffic_note"] = ("dram__bytes_read.sum + dram__bytes_write.sum per launch from the committed ncu "
                                 "capture of these kernel sources" if roofline["traffic"] is not None else
-                                "no ncu capture of the current kernel sources")
-    per_kernel = {k: {"launches": n, "total_ms": round(t, 4), "avg_us": round(t / n * 1e3, 2),
-                      "share": round(t / sum(v[0] for v in kernels.values()), 4)}
-                  for k, (t, n) in sorted(kernels.items(), key=lambda kv: -kv[1][0])}
+                                "no ncu capture of the current kernel sources for this workload")
 
     # ---- the same steps captured once in a CUDA graph and replayed: launch-amortised
     # time, reported beside (not instead of) the stream-launched value
-    graph = graph_timing(step, n_sets, flops, world, timed)
+    graph = graph_timing(wl.step, wl.n_sets, flops, world, timed)
 
     # ---- end to end: pinned host buffers, copies inside the timed region
-    t0 = sets[0]
-    hX = t0["X"].cpu().pin_memory()
-    hdY = t0["dY"].cpu().pin_memory()
-    hY = torch.empty_like(t0["Y"], device="cpu").pin_memory()
-    hdX = torch.empty_like(t0["dX"], device="cpu").pin_memory()
-    hdA = torch.empty_like(t0["dA"], device="cpu").pin_memory()
-    hdB = torch.empty_like(t0["dB"], device="cpu").pin_memory()
-    dX_in, dY_in = torch.empty_like(t0["X"]), torch.empty_like(t0["dY"])
+    e2e = e2e_timing(wl, args, timed, flops, world)
 
-    def e2e_step(i):
-        dX_in.copy_(hX, non_blocking=True)
-        if not only_fwd:
-            dY_in.copy_(hdY, non_blocking=True)
-        qlora.qlora_linear_fwd(dX_in, t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
-                               Y=t0["Y"], XA=t0["XA"], workspace=ws)
-        hY.copy_(t0["Y"], non_blocking=True)
-        if not only_fwd:
-            qlora.qlora_linear_bwd(dX_in, dY_in, t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
-                                   t0["XA"], dX=t0["dX"], dA=t0["dA"], dB=t0["dB"], workspace=ws)
-            hdX.copy_(t0["dX"], non_blocking=True)
-            hdA.copy_(t0["dA"], non_blocking=True)
-            hdB.copy_(t0["dB"], non_blocking=True)
+    codec = codec_rooflines(sh, wl.sets, dev, peaks)
 
-    e2e_step(0)
-    e2e_steps = max(3, min(args.steps, 200))
-    e2e_ms = timed(e2e_step, e2e_steps) / e2e_steps
-    h2d = hX.numel() * 2 + (0 if only_fwd else hdY.numel() * 2)
-    d2h = hY.numel() * 2 + (0 if only_fwd else hdX.numel() * 2 + hdA.numel() * 4 + hdB.numel() * 4)
-
-    codec = codec_rooflines(sh, sets, dev, peaks, stream)
+    extra = {}
+    if not args.no_extra:
+        del wl
+        torch.cuda.empty_cache()
+        for name in EXTRA_CONFIGS:
+            if name == sh.name:
+                continue
+            try:
+                extra[name] = measure_extra(shape_of(name), dev, rank, l2, peaks, timed, sampler)
+            except Exception as e:   # report, do not fail the run
+                extra[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
+    sampler.stop()
 
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return 0
 
+    tpk, tkind = tensor_peak(peaks, region_s)
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(sh),
-                   "l2": f"inputs rotated over {n_sets} resident sets of {set_bytes / 1e6:.0f} MB "
-                         f"(> 2x the {l2 / 1e6:.0f} MB L2)",
+        "config": {"workload": workload_desc(sh), "l2": e2e.pop("l2_note"),
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": tokens_per_s,
-        "frac_of_bf16_peak_whole_step": {"sustained": tflops_rank / peaks["bf16_sust"],
+        "frac_of_bf16_peak_whole_step": {"frac": tflops_rank / tpk, "peak_kind": tkind,
+                                         "sustained": tflops_rank / peaks["bf16_sust"],
                                          "burst": tflops_rank / peaks["bf16"]},
         "roofline": roofline,
         "kernels": per_kernel,
-        "profiled_ms_per_step": prof_total_ms / args.steps,
+        "profiled_ms_per_step": prof_ms,
         "gpu_launches": launches,
         "hbm_kernels": codec,
         "cuda_graph": graph,
         "clocks": clocks,
-        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "e2e": e2e,
+        "extra": extra,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(sh, min_seconds=args.cpu_seconds)
@@ -496,6 +674,45 @@ def run_ours(args):
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def e2e_timing(wl, args, timed, flops, world):
+    """Forward + backward through the public API from pinned host inputs to host
+    outputs, the copies inside the timed region."""
+    import torch
+    from rank_adapter_linear_nf4_b300 import qlora
+    sh, t0 = wl.sh, wl.sets[0]
+    hX = t0["X"].cpu().pin_memory()
+    hdY = None if wl.only_fwd else wl.dY0.cpu().pin_memory()
+    hY = torch.empty_like(t0["Y"], device="cpu").pin_memory()
+    hdX = None if wl.only_fwd else torch.empty_like(t0["dX"], device="cpu").pin_memory()
+    hdA = torch.empty_like(t0["dA"], device="cpu").pin_memory()
+    hdB = torch.empty_like(t0["dB"], device="cpu").pin_memory()
+    X_in = torch.empty_like(t0["X"])
+    dY_in = None if wl.only_fwd else torch.empty_like(wl.dY0)
+
+    def e2e_step(i):
+        X_in.copy_(hX, non_blocking=True)
+        if not wl.only_fwd:
+            dY_in.copy_(hdY, non_blocking=True)
+        qlora.qlora_linear_fwd(X_in, t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
+                               Y=t0["Y"], XA=t0["XA"], workspace=wl.ws)
+        hY.copy_(t0["Y"], non_blocking=True)
+        if not wl.only_fwd:
+            qlora.qlora_linear_bwd(X_in, dY_in, t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
+                                   t0["XA"], dX=t0["dX"], dA=t0["dA"], dB=t0["dB"], workspace=wl.ws)
+            hdX.copy_(t0["dX"], non_blocking=True)
+            hdA.copy_(t0["dA"], non_blocking=True)
+            hdB.copy_(t0["dB"], non_blocking=True)
+
+    e2e_step(0)
+    steps = max(3, min(args.steps, 200))
+    ms = timed(e2e_step, steps)[0] / steps
+    h2d = hX.numel() * 2 + (0 if wl.only_fwd else hdY.numel() * 2)
+    d2h = hY.numel() * 2 + (0 if wl.only_fwd else hdX.numel() * 2 + hdA.numel() * 4 + hdB.numel() * 4)
+    return {"value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
+            "l2_note": wl.l2_note()}
 
 
 def graph_timing(step, n_sets, flops, world, timed, replays=20):
@@ -516,14 +733,14 @@ def graph_timing(step, n_sets, flops, world, timed, replays=20):
                 step(i)
         g.replay()
         torch.cuda.synchronize()
-        ms = timed(lambda i: g.replay(), replays) / (replays * per_graph)
+        ms = timed(lambda i: g.replay(), replays)[0] / (replays * per_graph)
     except Exception as e:   # report, do not fail the run
         return {"error": f"{type(e).__name__}: {e}"[:200]}
     return {"ms_per_step": ms, "value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "steps_per_graph": per_graph, "replays": replays}
 
 
-def codec_rooflines(sh, sets, dev, peaks, stream, reps=20):
+def codec_rooflines(sh, sets, dev, peaks, reps=20):
     """The HBM-bound kernels beside the layer, each timed alone with CUDA events,
     alternating two inputs (> L2 together): NF4 quantise and dequantise of this
     workload's weight (rows a1, a2), the merged weight bf16(W_deq + s.(A.B)^T)
@@ -537,11 +754,12 @@ def codec_rooflines(sh, sets, dev, peaks, stream, reps=20):
     pk = [torch.empty_like(t["packed"]) for t in sets[:2]]
     am = [torch.empty_like(t["absmax"]) for t in sets[:2]]
     g = torch.Generator(device=dev).manual_seed(5)
-    gus = [torch.randn(sh.M, 2 * sh.d_out, device=dev, generator=g).to(torch.bfloat16) for _ in range(2)]
-    dhs = [torch.randn(sh.M, sh.d_out, device=dev, generator=g).to(torch.bfloat16) for _ in range(2)]
+    m_rows = max(sh.M, 1024)
+    gus = [torch.randn(m_rows, 2 * sh.d_out, device=dev, generator=g).to(torch.bfloat16) for _ in range(2)]
+    dhs = [torch.randn(m_rows, sh.d_out, device=dev, generator=g).to(torch.bfloat16) for _ in range(2)]
     hs = [torch.empty_like(d) for d in dhs]
     dgus = [torch.empty_like(x) for x in gus]
-    m_ff = sh.M * sh.d_out
+    m_ff = m_rows * sh.d_out
     res = {}
     for name, fn, nbytes, elems in (
             ("nf4_quantize", lambda i: qlora.qlora_quantize_nf4(Ws[i % 2], packed=pk[i % 2], absmax=am[i % 2]),
@@ -573,18 +791,23 @@ def codec_rooflines(sh, sets, dev, peaks, stream, reps=20):
         res[name] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm"], "avg_launch_us": us,
                      "algorithmic_bytes_per_launch": nbytes, "elements": elems}
+    del Ws, outs, pk, am, gus, dhs, hs, dgus
+    torch.cuda.empty_cache()
     return res
 
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="measure the headline workload only")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--only-steps", action="store_true",
+                    help="run the warm-up and the timed steps only (for profiler launch lists and captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

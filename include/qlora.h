@@ -39,7 +39,11 @@
  *     cudaError_t value;
  *   - every device-side wait is bounded (about one second); a wait that runs
  *     out records QLORA_ERR_TIMEOUT in a device status word read by
- *     qlora_device_status(); the kernel then returns without finishing.
+ *     qlora_device_status(); the kernel then returns without finishing;
+ *   - the library caches, per device, the device addresses of its own device
+ *     variables (the status word, the no-allocation scratch array); do not
+ *     keep using a loaded library across cudaDeviceReset() or a reset of the
+ *     primary context, which moves them.
  */
 #ifndef QLORA_H_
 #define QLORA_H_
@@ -199,9 +203,11 @@ qlora_status qlora_linear_fwd(const uint16_t* X, int64_t M, int64_t d_in, int64_
  * start-up, or glue code that only holds the layer's own tensors.  Its
  * scratch is a fixed 8 MiB device array inside this library, which every GPU
  * that loads the library keeps for the life of the process.
- *   - Needs (d_in + M) * rp * 2 bytes of that array, rp = 64 * ceil(r / 64)
- *     (each part rounded up to 1 KiB); larger shapes return
- *     QLORA_ERR_WORKSPACE and launch nothing.
+ *   - Needs M * rp * 2 bytes of that array, plus d_in * rp * 2 bytes when
+ *     r % 8 != 0 (a zero-padded copy of A), rp = 64 * ceil(r / 64), each part
+ *     rounded up to 1 KiB; larger shapes return QLORA_ERR_WORKSPACE and launch
+ *     nothing.  What is left of the array holds the split-work counters and
+ *     partial tiles; with too little left the kernels fall back to whole tiles.
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and caches it; make that first call before any
  *     stream capture.

@@ -17,7 +17,10 @@ thread_local int g_last_cuda_error = 0;
 __device__ int g_device_status;
 
 constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices] = {nullptr};
+// Per-device cache of the status word's address; filled under g_status_mu so
+// that threads making their first call on a device at once do not race.
+std::mutex g_status_mu;
+std::atomic<int*> g_status_ptr[kMaxDevices] = {};
 
 qlora_status cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
@@ -30,13 +33,19 @@ qlora_status status_word(int** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
   if (dev < 0 || dev >= kMaxDevices) return QLORA_ERR_UNSUPPORTED;
-  if (g_status_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_device_status);
-    if (e != cudaSuccess) return cuda_fail(e);
-    g_status_ptr[dev] = static_cast<int*>(p);
+  int* word = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (word == nullptr) {
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    word = g_status_ptr[dev].load(std::memory_order_relaxed);
+    if (word == nullptr) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_device_status);
+      if (e != cudaSuccess) return cuda_fail(e);
+      word = static_cast<int*>(p);
+      g_status_ptr[dev].store(word, std::memory_order_release);
+    }
   }
-  *out = g_status_ptr[dev];
+  *out = word;
   return QLORA_OK;
 }
 

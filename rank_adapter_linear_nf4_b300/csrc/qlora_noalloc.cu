@@ -25,8 +25,9 @@
 
 namespace {
 
-// 8 MiB: enough for (d_in + M) * rp * 2 bytes with rp = 64*ceil(r/64), e.g.
-// M = 16384 tokens, d_in = 14336, r = 128.
+// 8 MiB: enough for M * rp * 2 bytes (plus d_in * rp * 2 when r % 8 != 0) with
+// rp = 64*ceil(r/64), e.g. M = 16384 tokens at r = 128, or M = 16384 tokens and
+// d_in = 14336 at r = 100.
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
@@ -83,8 +84,9 @@ extern "C" qlora_status qlora_linear_fwd_noalloc(const uint16_t* X, int64_t M, i
   d.r = r;
   d.rp = (r + 63) / 64 * 64;
   d.s = s;
-  // the forward reads and writes two scratch regions: padded A [d_in, rp] and bf16(s*T) [M, rp]
-  const size_t a_pad_bytes = round_up_1k(static_cast<size_t>(d.K) * d.rp * 2);
+  // the forward reads and writes bf16(s*T) [M, rp] and, only for ranks whose
+  // rows are not 16-byte multiples (r % 8 != 0), a zero-padded copy of A [d_in, rp]
+  const size_t a_pad_bytes = (d.r % 8 != 0) ? round_up_1k(static_cast<size_t>(d.K) * d.rp * 2) : 0;
   const size_t s_t_bytes = round_up_1k(static_cast<size_t>(d.M) * d.rp * 2);
   if (a_pad_bytes + s_t_bytes > kNoAllocScratchBytes) return QLORA_ERR_WORKSPACE;
 
@@ -99,15 +101,19 @@ extern "C" qlora_status qlora_linear_fwd_noalloc(const uint16_t* X, int64_t M, i
   if (status == nullptr) return QLORA_ERR_CUDA;
 
   qlora::Workspace ws;
-  ws.a_pad = static_cast<uint16_t*>(scratch);
+  ws.a_pad = a_pad_bytes != 0 ? static_cast<uint16_t*>(scratch) : nullptr;
   ws.s_t = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(scratch) + a_pad_bytes);
   ws.s_g = nullptr;   // backward only
   // what is left of the array holds the counters and partial tiles of the
   // main kernel and the token-stream kernel; without them the main kernel
   // takes whole tiles only
   int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    qlora::record_cuda_error(static_cast<int>(e));
+    return QLORA_ERR_CUDA;
+  }
   const int n_counters = std::max(sms, qlora::stream_counter_slots(d));
   const size_t counter_bytes = round_up_1k(static_cast<size_t>(n_counters) * sizeof(int));
   const size_t used = a_pad_bytes + s_t_bytes;

@@ -1,11 +1,13 @@
-"""The allocation-free forward (qlora_linear_fwd_noalloc) against the ordinary one.
+"""The allocation-free forward (qlora_linear_fwd_noalloc) against the ordinary one
+and against the oracle.
 
 The no-workspace entry point exists for callers that cannot hand the layer a
 scratch buffer (another allocator owns the device memory, or nothing may be
 allocated after start-up).  Its scratch is a fixed array inside the library
 that every call reuses, so these checks call it twice in a row on the same
-stream and compare both results with qlora_linear_fwd, through the C ABI.
-This file is collected last on purpose; it also passes when run on its own.
+stream and compare both results with qlora_linear_fwd, through the C ABI, and
+with the CPU oracle on sampled rows.  This file is collected last on purpose;
+it also passes when run on its own.
 """
 import ctypes
 
@@ -13,8 +15,9 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import qlora_oracle as O
 from rank_adapter_linear_nf4_b300 import synthetic
-from tests.parity_utils import TOL, rel_max_err
+from tests.parity_utils import TOL, np32, oracle_weight, rel_max_err
 
 pytestmark = pytest.mark.gpu
 
@@ -51,17 +54,23 @@ def test_noalloc_forward_matches_workspace_forward_twice(case):
     X, W, A, B = X.to(dev), W.to(dev), A.to(dev), B.to(dev)
     packed, absmax = qlora.qlora_quantize_nf4(W)
     Y_ref, XA_ref = qlora.qlora_linear_fwd(X, packed, absmax, A, B, s)
+    # the oracle on sampled rows (all rows for the small cases)
+    rows = synthetic.sample_rows(M, n=64, block=32) if M > 512 else None
+    _, _, Wd = oracle_weight(W.cpu())
+    Y_o, T_o = O.lora_forward(np32(X), Wd, np32(A), np32(B), s, rows=rows)
+    sel = slice(None) if rows is None else rows
     for call in range(2):
         Y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=dev)
         XA = torch.full((M, r), float("nan"), dtype=torch.float32, device=dev)
         assert _noalloc_call(lib, X, packed, absmax, A, B, s, Y, XA) == QLORA_OK
         torch.cuda.synchronize()
         assert qlora.qlora_device_status(clear=True) == 0
-        for name, got, ref in (("Y", Y, Y_ref), ("XA", XA, XA_ref)):
+        for name, got, ref, orc in (("Y", Y, Y_ref, Y_o), ("XA", XA, XA_ref, T_o)):
             g = got.float().cpu().numpy()
             r_ = ref.float().cpu().numpy()
             assert np.all(np.isfinite(g)), (call, name)
             assert rel_max_err(g, r_) <= TOL, (call, name)
+            assert rel_max_err(g[sel], orc) <= TOL, (call, name, "oracle")
 
 
 def test_noalloc_rejects_shapes_beyond_its_array():
