@@ -337,19 +337,39 @@ def cpu_baseline(sh, min_seconds=10.0):
            "sample": f"{tokens} of {sh.M} tokens of the same workload (NF4 dequantise of the full "
                      f"weight + fp64 forward{'' if fwd_only(sh) else ' + backward'}), median of {calls} calls, "
                      f"{per_call * 1e3:.1f} ms per call, {threads} BLAS threads"}
-    try:
-        from threadpoolctl import threadpool_limits
-        t1 = min(sh.M, 32)
-        r1 = OracleRunner(sh, t1)
-        with threadpool_limits(limits=1):
-            pc1, c1 = r1.time_calls(min_seconds / 2)
-        f1 = step_flops(sample_shape(sh, t1))
-        out["single_thread"] = {"value": f1 / pc1 / 1e12, "unit": "TFLOP/s", "cores": 1,
-                                "tokens_per_s": t1 / pc1,
-                                "sample": f"{t1} tokens, median of {c1} calls, {pc1 * 1e3:.1f} ms per call"}
-    except Exception as e:   # report, do not fail the run
-        out["single_thread"] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    out["single_thread"] = single_thread_baseline(sh, min_seconds / 2)
     return out
+
+
+SINGLE_THREAD_ENV = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS")
+
+
+def single_thread_baseline(sh, min_seconds):
+    """The oracle on one core: a child process with every BLAS thread count set
+    to 1 before numpy loads (32 tokens of the workload)."""
+    import subprocess
+    env = dict(os.environ, **{k: "1" for k in SINGLE_THREAD_ENV})
+    env.pop("RANK", None)
+    cmd = [sys.executable, os.path.abspath(__file__), "--single-thread-probe", "--config", sh.name,
+           "--cpu-seconds", str(min_seconds)]
+    try:
+        res = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+        return json.loads(res.stdout.strip().splitlines()[-1])
+    except Exception as e:   # report, do not fail the run
+        return {"error": f"{type(e).__name__}: {e}"[:200]}
+
+
+def run_single_thread_probe(args):
+    sh = shape_of(args.config)
+    tokens = min(sh.M, 32)
+    runner = OracleRunner(sh, tokens)
+    per_call, calls = runner.time_calls(args.cpu_seconds)
+    flops = step_flops(sample_shape(sh, tokens))
+    print(json.dumps({"value": flops / per_call / 1e12, "unit": "TFLOP/s", "cores": 1,
+                      "tokens_per_s": tokens / per_call,
+                      "sample": f"{tokens} tokens, median of {calls} calls, {per_call * 1e3:.1f} ms per call, "
+                                f"BLAS threads 1 ({', '.join(SINGLE_THREAD_ENV)})"}))
+    return 0
 
 
 # ---------------------------------------------------------------- multi-rank helpers
@@ -476,20 +496,28 @@ def make_timer(stream, world, dev, barrier):
     return timed
 
 
-def per_kernel_profile(wl, steps, timed):
+# Idle time before the per-kernel region, so that it starts from the same power
+# state as the timed region before it (a second burst right after the first runs
+# under the power cap).
+COOL_DOWN_S = 1.0
+
+
+def per_kernel_profile(wl, steps, timed, sampler):
     """The same steps with every library launch bracketed by CUDA events on its
-    stream: per kind, launches, total ms, average us, share."""
+    stream: per kind, launches, total ms, average us, share; and the clocks of
+    that region."""
     from rank_adapter_linear_nf4_b300 import qlora
+    time.sleep(COOL_DOWN_S)
     qlora.qlora_profile_enable(True)
     qlora.qlora_profile_collect()
-    prof_ms, _, _ = timed(wl.step, steps)
+    prof_ms, h0, h1 = timed(wl.step, steps)
     kernels = qlora.qlora_profile_collect()
     qlora.qlora_profile_enable(False)
     total = sum(v[0] for v in kernels.values())
     per = {k: {"launches": n, "total_ms": round(t, 4), "avg_us": round(t / n * 1e3, 2),
                "share": round(t / total, 4)}
            for k, (t, n) in sorted(kernels.items(), key=lambda kv: -kv[1][0])}
-    return per, prof_ms / steps
+    return per, prof_ms / steps, sampler.summary(h0, h1)
 
 
 def kernel_roofline(sh, name, avg_us, peaks, region_s):
@@ -537,7 +565,7 @@ def measure_extra(sh, dev, rank, l2, peaks, timed, sampler, target_s=0.15, warmu
     steps = int(max(10, min(2000, target_s / (est_ms / 3 * 1e-3))))
     total_ms, h0, h1 = timed(wl.step, steps)
     ms = total_ms / steps
-    kernels, prof_ms = per_kernel_profile(wl, steps, timed)
+    kernels, prof_ms, prof_clocks = per_kernel_profile(wl, steps, timed, sampler)
     flops, nbytes = step_flops(sh), step_bytes(sh)
     region_s = total_ms * 1e-3
     tpk, tkind = tensor_peak(peaks, region_s)
@@ -548,6 +576,7 @@ def measure_extra(sh, dev, rank, l2, peaks, timed, sampler, target_s=0.15, warmu
            "step_hbm_gbs": nbytes / (ms * 1e-3) / 1e9, "step_frac_of_hbm": nbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
            "dominant": kernel_roofline(sh, dom, kernels[dom]["avg_us"], peaks, region_s),
            "kernels": kernels, "profiled_ms_per_step": prof_ms, "clocks": sampler.summary(h0, h1),
+           "profiled_clocks": prof_clocks,
            "l2": wl.l2_note()}
     del wl
     torch.cuda.empty_cache()
@@ -611,7 +640,7 @@ def run_ours(args):
         return 0
 
     # ---- same region again with every library launch bracketed by CUDA events
-    per_kernel, prof_ms = per_kernel_profile(wl, args.steps, timed)
+    per_kernel, prof_ms, prof_clocks = per_kernel_profile(wl, args.steps, timed, sampler)
     roof_kind = dominant_layer_kernel(per_kernel)
     roofline = kernel_roofline(sh, roof_kind, per_kernel[roof_kind]["avg_us"], peaks, region_s)
     roofline["traffic"] = stored_traffic(roof_kind, sh.name)
@@ -661,6 +690,7 @@ def run_ours(args):
         "roofline": roofline,
         "kernels": per_kernel,
         "profiled_ms_per_step": prof_ms,
+        "profiled_clocks": prof_clocks,
         "gpu_launches": launches,
         "hbm_kernels": codec,
         "cuda_graph": graph,
@@ -806,11 +836,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="measure the headline workload only")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--single-thread-probe", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--only-steps", action="store_true",
                     help="run the warm-up and the timed steps only (for profiler launch lists and captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.single_thread_probe:
+        return run_single_thread_probe(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -75,7 +75,8 @@ size_t workspace_bytes(const LayerDims& d);
 // Counters the workspace holds: the main kernel's split tiles (one per SM) or
 // the token-stream kernel's 64-row panels, whichever is more.
 int counter_slots(const LayerDims& d);
-// Bytes of partial tiles the main kernel uses at most for these dimensions.
+// Bytes of partial tiles the main kernel, or for at most kStreamMaxTokens
+// tokens the token-stream kernel, uses at most for these dimensions.
 size_t split_partial_bytes(const LayerDims& d);
 Workspace carve_workspace(const LayerDims& d, void* base);
 
@@ -84,11 +85,11 @@ cudaError_t run_forward(const LayerDims& d, const uint16_t* X, const uint8_t* pa
                         float* XA, const Workspace& ws, int* status, cudaStream_t stream);
 
 // Forward for at most kStreamMaxTokens tokens as a stream of the NF4 weight
-// (lora_stream.cu); it needs counter_slots(d) counters and partial panels for
-// two per CTA in the workspace.
+// (lora_stream.cu); it needs stream_counter_slots(d) counters (one per 32-row
+// pair) and stream_partial_bytes(d, sms) of partial slots in the workspace.
 constexpr int kStreamMaxTokens = 16;
 int stream_counter_slots(const LayerDims& d);
-size_t stream_partial_bytes(int grid);
+size_t stream_partial_bytes(const LayerDims& d, int sms);
 bool stream_applies(const LayerDims& d, const Workspace& ws, int sms);
 cudaError_t launch_stream_fwd(const LayerDims& d, const uint16_t* X, const uint8_t* packed, const float* absmax,
                               const uint16_t* B, const Workspace& ws, uint16_t* Y, int* status, int sms,

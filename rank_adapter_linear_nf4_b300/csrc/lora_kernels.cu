@@ -1212,7 +1212,10 @@ bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* gadd
 }
 
 size_t split_partial_bytes(const LayerDims& d) {
-  return static_cast<size_t>(2) * sm_count() * kTileP * pick_bn(d.M) * sizeof(float);
+  const int sms = sm_count();
+  const size_t main_bytes = static_cast<size_t>(2) * sms * kTileP * pick_bn(d.M) * sizeof(float);
+  if (d.M > kStreamMaxTokens) return main_bytes;
+  return std::max(main_bytes, stream_partial_bytes(d, sms));
 }
 
 int counter_slots(const LayerDims& d) { return std::max(sm_count(), stream_counter_slots(d)); }

@@ -90,8 +90,8 @@ def test_token_sweep(m):
 # contractions), so partial tiles are summed by the last CTA to finish them;
 # the last one also has whole-tile rounds before the split remainder.
 SPLIT = [
-    (16, 4096, 256, 16, 1.0),      # Y: 2 tiles x 65 stages over 8 CTAs
-    (16, 256, 4096, 16, 0.5),      # dX: 2 tiles x 65 stages
+    (24, 4096, 256, 16, 1.0),      # Y: 2 tiles x 65 stages over 8 CTAs (BN 32)
+    (16, 256, 4096, 16, 0.5),      # dX: 2 tiles x 65 stages (Y through the token-stream kernel)
     (40, 4096, 392, 24, 2.0),      # Y: BN 64, ragged feature tile, padded rank
     (300, 2048, 10240, 16, 1.0),   # Y: 160 tiles = one whole round + 12 split tiles
 ]

@@ -1,11 +1,11 @@
 """The forward for 1..16 tokens (the NF4 weight-stream kernel) against the oracle.
 
 Same bar as the other layer tests: per output tensor, max|gpu - oracle| <=
-1e-2 * max|oracle|, every element compared.  The cases walk the kernel's two
-schedules: whole 64-row panels per CTA (at least as many panels as SMs, the
-last panel ragged) and stages split evenly with panels shared by CTAs (a
-panel over many CTAs, each one stage; whole panels inside one CTA next to
-split ones); ranks 1..128 and token counts on both sides of 8.
+1e-2 * max|oracle|, every element compared.  The kernel splits the items
+(32 weight rows x one 64-element block) evenly over its warps; the cases walk
+ranges inside one row pair, ranges crossing several row pairs (short d_in),
+row pairs shared by many warps (long d_in), ragged last pairs (d_out % 32 !=
+0), ranks 1..128 and token counts on both sides of 8.
 Low-rank-dominant cases (zero base weight, B ~ N(0, 1)) check that term on its
 own, since with the standard scales it is only a few percent of Y.
 """
@@ -25,17 +25,20 @@ def _inputs(M, K, N, r, seed=0, b_std=0.01):
 
 
 CASES = [
-    # (M, d_in, d_out, r, s); d_in is a multiple of 256 (one stage = 64 rows x 256 features)
-    (1, 256, 256, 16, 1.0),         # four panels of one stage: one CTA each
-    (3, 256, 64, 8, 2.0),           # a single stage, a single CTA
-    (8, 4096, 64, 16, 1.0),         # one panel of 16 stages, one stage per CTA: 16 pieces summed
-    (9, 512, 136, 24, 0.5),         # two token groups with 9 tokens; 3 panels (the last 8 rows) split in two
-    (16, 512, 14336, 128, 0.25),    # whole panels within CTAs beside split ones; rank 128
-    (5, 14336, 256, 64, 0.25),      # long contraction: 4 panels of 56 stages
+    # (M, d_in, d_out, r, s); an item is 32 weight rows x one 64-element block
+    (1, 256, 256, 16, 1.0),         # 8 row pairs of 4 items: one warp's range spans row pairs
+    (3, 256, 64, 8, 2.0),           # a single CTA
+    (8, 4096, 64, 16, 1.0),         # two row pairs of 64 items, each summed over several warps
+    (9, 512, 136, 24, 0.5),         # two token groups with 9 tokens; last row pair has 8 rows
+    (16, 512, 14336, 128, 0.25),    # 448 row pairs; rank 128
+    (5, 14336, 256, 64, 0.25),      # long contraction: 8 row pairs of 224 items, ~56 warps each
     (16, 4096, 4096, 16, 1.0),      # the q_proj layer at 16 tokens
-    (12, 512, 200, 65, 1.25),       # rank padded to 128, A padded (r % 8 != 0), last panel 8 rows
-    (2, 256, 8, 1, 3.0),            # one 8-row panel, rank 1
-    (4, 1024, 64 * 148 + 8, 16, 0.5),   # 149 panels, whole panels per CTA, the last one 8 rows
+    (12, 512, 200, 65, 1.25),       # rank padded to 128, A padded (r % 8 != 0), last pair 8 rows
+    (2, 256, 8, 1, 3.0),            # one 8-row pair (24 rows past d_out), rank 1
+    (4, 1024, 64 * 148 + 8, 16, 0.5),   # 297 row pairs, the last one 8 rows
+    (7, 64, 14336, 32, 0.5),        # one block per row: each warp's range crosses 4 row pairs
+    (16, 320, 96, 48, 1.0),         # d_in % 256 != 0
+    (1, 192, 40, 4, 2.0),           # d_in = 3 blocks, last pair 8 rows
 ]
 
 
@@ -62,9 +65,9 @@ def test_stream_with_backward():
 def test_stream_kernel_is_the_one_launched():
     from rank_adapter_linear_nf4_b300 import qlora
     dev = torch.device("cuda", 0)
-    # 1..16 tokens with d_in % 256 == 0 take the stream kernel, the rest the main kernel
+    # 1..16 tokens take the stream kernel, more tokens the main kernel
     for M, K, want, other in ((16, 256, "lora_stream_fwd", "lora_main_fwd"), (17, 256, "lora_main_fwd", "lora_stream_fwd"),
-                              (4, 320, "lora_main_fwd", "lora_stream_fwd")):
+                              (4, 320, "lora_stream_fwd", "lora_main_fwd")):
         inp = _inputs(M, K, 256, 16, seed=M)
         X, W, A, B = (inp[k].to(dev) for k in ("X", "W", "A", "B"))
         packed, absmax = qlora.qlora_quantize_nf4(W)
@@ -79,8 +82,8 @@ def test_stream_kernel_is_the_one_launched():
 
 
 def test_stream_repeat_is_bitwise_identical():
-    """Split panels are summed by whichever CTA arrives last, in CTA order:
-    repeated calls give the same bits."""
+    """Row pairs shared by warps are summed by whichever warp arrives last, in
+    warp order: repeated calls give the same bits."""
     inp = _inputs(16, 4096, 14336, 64, seed=2)
     a = run_gpu(inp, 0.25, bwd=False)
     for _ in range(3):
