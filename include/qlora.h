@@ -98,6 +98,17 @@ qlora_status qlora_profile_enable(int enable);
 int qlora_profile_collect(const char** names, float* total_ms, int* launches, int max_kinds);
 int64_t qlora_launch_count(void);
 
+/* Test hook for the error path of the bounded device waits (off by default;
+ * an interface addition of this library, with no counterpart on the pages).
+ * The next `launches` launches of the fused main kernel (the forward Y for
+ * more than 16 tokens, the backward dX) load no token operand: no stage
+ * completes, the waits run out after about one second, the kernel records
+ * QLORA_ERR_TIMEOUT in the status word (qlora_device_status), releases its
+ * tensor memory and returns with nothing in flight; its output is left
+ * unwritten or partly written.  0 switches the hook off.  Returns
+ * QLORA_ERR_SHAPE for a negative count. */
+qlora_status qlora_debug_stall_main_launches(int launches);
+
 /*
  * NF4 quantisation of a bf16 weight (offline; once per weight).
  *   W       [n_out, n_in] bf16, read.
@@ -241,6 +252,88 @@ qlora_status qlora_linear_bwd(const uint16_t* X, const uint16_t* dY,
                               uint16_t* dX, float* dA, float* dB,
                               void* workspace, size_t workspace_bytes,
                               qlora_stream_t stream);
+
+/*
+ * SwiGLU MLP block with the gate fused into the layers' epilogues.
+ *
+ *     gu = X . W_gu_deq^T + s_gu . (X . A_gu) . B_gu      (gate and up projections, one layer)
+ *     h  = silu(g) * u,   silu(x) = x / (1 + e^-x)
+ *     Y  = h . W_d_deq^T + s_d . (h . A_d) . B_d          (down projection)
+ *
+ * The pages fuse the MLP of the transformer block into their forward
+ * ("Unsloth性能实测：比传统方法快2倍真的吗？", section 2.2) and name SwiGLU among the
+ * fused transformer operators ("UnSloth加速原理：CUDA内核融合与内存优化", section
+ * "在ms-swift中的角色").  Here the gate costs no pass of its own: the gate/up
+ * layer's epilogue writes h beside gu, and the down layer's backward epilogue
+ * turns its input gradient dh into dgu (the gate's backward) without storing dh.
+ *
+ * Layout of the gate/up layer (d_in -> 2*d_ff, d_ff % 64 == 0): its weight rows,
+ * the columns of B_gu and the columns of gu are INTERLEAVED in 64-row chunks,
+ *     [gate 0..63 | up 0..63 | gate 64..127 | up 64..127 | ...],
+ * so that every 128-feature output tile holds matching gate and up features.
+ * Quantise the interleaved bf16 weight with qlora_quantize_nf4 (NF4 blocks lie
+ * within a row, so its codes are the separate weights' codes, rows permuted).
+ * Rounding: gu, h, dh and dgu are rounded to bf16 at the points where an
+ * unfused block stores them, and the gate's arithmetic is fp32, so the fused
+ * block computes what the unfused one (qlora_linear_* + qlora_swiglu_*) does.
+ */
+
+/* Forward of the interleaved gate/up layer: gu [M, 2*d_ff] (the layer's Y) and
+ * h [M, d_ff], both bf16, written; XA_save [M, r] fp32 written (T for the
+ * backward).  Other arguments and requirements as qlora_linear_fwd with
+ * d_out = 2*d_ff; d_ff % 64 == 0.  For 1..16 tokens the gate is a separate
+ * elementwise pass after the weight-stream kernel. */
+qlora_status qlora_linear_fwd_swiglu(const uint16_t* X, int64_t M, int64_t d_in, int64_t d_ff,
+                                     const uint8_t* packed, const float* absmax,
+                                     const uint16_t* A, const uint16_t* B, int32_t r, float s,
+                                     uint16_t* gu, uint16_t* h, float* XA_save,
+                                     void* workspace, size_t workspace_bytes, qlora_stream_t stream);
+
+/* Backward of the down layer (d_ff -> d_out) of the block: as qlora_linear_bwd
+ * with X = h, except that the layer's input gradient dh is not stored;
+ * instead dgu [M, 2*d_ff] bf16 (interleaved like gu) is written,
+ *   dgu[gate f] = dh * u * sigma(g) * (1 + g * (1 - sigma(g))),  dgu[up f] = dh * silu(g),
+ * from gu [M, 2*d_ff] (read, the forward's).  dA, dB as in qlora_linear_bwd. */
+qlora_status qlora_linear_bwd_swiglu(const uint16_t* h, const uint16_t* dY, int64_t M, int64_t d_ff,
+                                     int64_t d_out, const uint8_t* packed, const float* absmax,
+                                     const uint16_t* A, const uint16_t* B, int32_t r, float s,
+                                     const float* XA_saved, const uint16_t* gu, uint16_t* dgu,
+                                     float* dA, float* dB, void* workspace, size_t workspace_bytes,
+                                     qlora_stream_t stream);
+
+/* Workspace for qlora_swiglu_mlp_fwd / _bwd (the larger of the two layers'); 0 if unsupported. */
+size_t qlora_swiglu_mlp_workspace_bytes(int64_t M, int64_t d_model, int64_t d_ff, int32_t r_gu, int32_t r_d);
+
+/* The whole block forward: qlora_linear_fwd_swiglu, then the down layer.
+ *   X [M, d_model] read; Y [M, d_model] written; gu [M, 2*d_ff], h [M, d_ff],
+ *   T_gu [M, r_gu], T_d [M, r_d] written (saved for the backward).
+ *   gate/up layer: gu_packed, gu_absmax (interleaved [2*d_ff, d_model] weight),
+ *   A_gu [d_model, r_gu], B_gu [r_gu, 2*d_ff] (interleaved columns), s_gu;
+ *   down layer: d_packed, d_absmax ([d_model, d_ff] weight), A_d [d_ff, r_d],
+ *   B_d [r_d, d_model], s_d.
+ * Requires d_model % 64 == 0, d_ff % 64 == 0, ranks in [1, 128]. */
+qlora_status qlora_swiglu_mlp_fwd(const uint16_t* X, int64_t M, int64_t d_model, int64_t d_ff,
+                                  const uint8_t* gu_packed, const float* gu_absmax, const uint16_t* A_gu,
+                                  const uint16_t* B_gu, int32_t r_gu, float s_gu,
+                                  const uint8_t* d_packed, const float* d_absmax, const uint16_t* A_d,
+                                  const uint16_t* B_d, int32_t r_d, float s_d,
+                                  uint16_t* Y, uint16_t* gu, uint16_t* h, float* T_gu, float* T_d,
+                                  void* workspace, size_t workspace_bytes, qlora_stream_t stream);
+
+/* The whole block backward: qlora_linear_bwd_swiglu (down layer, writes dgu),
+ * then the gate/up layer's backward with dY = dgu.
+ *   X, dY [M, d_model] read; gu, h, T_gu, T_d from the forward, read;
+ *   dgu [M, 2*d_ff] bf16: caller scratch, written; dX [M, d_model] bf16 written
+ *   (may be NULL to skip); dA_gu, dB_gu, dA_d, dB_d fp32 written (overwritten).
+ * Same layer arguments and requirements as qlora_swiglu_mlp_fwd. */
+qlora_status qlora_swiglu_mlp_bwd(const uint16_t* X, const uint16_t* dY, int64_t M, int64_t d_model, int64_t d_ff,
+                                  const uint8_t* gu_packed, const float* gu_absmax, const uint16_t* A_gu,
+                                  const uint16_t* B_gu, int32_t r_gu, float s_gu,
+                                  const uint8_t* d_packed, const float* d_absmax, const uint16_t* A_d,
+                                  const uint16_t* B_d, int32_t r_d, float s_d,
+                                  const uint16_t* gu, const uint16_t* h, const float* T_gu, const float* T_d,
+                                  uint16_t* dgu, uint16_t* dX, float* dA_gu, float* dB_gu, float* dA_d,
+                                  float* dB_d, void* workspace, size_t workspace_bytes, qlora_stream_t stream);
 
 #ifdef __cplusplus
 }

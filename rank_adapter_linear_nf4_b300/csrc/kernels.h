@@ -23,6 +23,7 @@ enum KernelKind : int {
   kKindStream,
   kKindSwigluFwd,
   kKindSwigluBwd,
+  kKindStreamFinish,
   kNumKernelKinds
 };
 
@@ -42,6 +43,10 @@ int* device_status_word(int* cuda_error);
 
 // Makes qlora_last_cuda_error() report `cuda_error` on the calling thread.
 void record_cuda_error(int cuda_error);
+
+// Test hook (qlora_debug_stall_main_launches): true for each of the next n
+// launches of the fused main kernel, which then loads no token operand.
+bool take_debug_stall();
 
 // NF4 codec (nf4_codec.cu).
 cudaError_t launch_quantize_nf4(const uint16_t* W, int64_t n_elems, uint8_t* packed, float* absmax,
@@ -80,17 +85,35 @@ int counter_slots(const LayerDims& d);
 size_t split_partial_bytes(const LayerDims& d);
 Workspace carve_workspace(const LayerDims& d, void* base);
 
+// The SwiGLU gate fused into a layer's epilogue (rows of W and columns of the
+// output interleaved in 64-row chunks, gate then up): the gate/up layer's
+// forward also writes h (h != nullptr); the down layer's backward writes dgu
+// from its dX and gu instead of storing dX (dgu != nullptr).
+struct GateIo {
+  uint16_t* h = nullptr;
+  const uint16_t* gu = nullptr;
+  uint16_t* dgu = nullptr;
+};
+
+// gate_h: nullptr, or h [M, N/2] for a gate/up layer with interleaved rows.
 cudaError_t run_forward(const LayerDims& d, const uint16_t* X, const uint8_t* packed,
                         const float* absmax, const uint16_t* A, const uint16_t* B, uint16_t* Y,
-                        float* XA, const Workspace& ws, int* status, cudaStream_t stream);
+                        float* XA, const Workspace& ws, int* status, cudaStream_t stream,
+                        uint16_t* gate_h = nullptr);
 
 // Forward for at most kStreamMaxTokens tokens as a stream of the NF4 weight
-// (lora_stream.cu); it needs stream_counter_slots(d) counters (one per 32-row
-// pair) and stream_partial_bytes(d, sms) of partial slots in the workspace.
+// (lora_stream.cu): the stream kernel, then a finishing kernel; it needs
+// stream_partial_bytes(d, sms) of partial slots in the workspace.
 constexpr int kStreamMaxTokens = 16;
+// SMs the token-stream kernel leaves to the rank-r kernel before it (one
+// 128-row tile, a cluster of at most 8 CTAs), which it overlaps.
+constexpr int kStreamReservedSms = 8;
 int stream_counter_slots(const LayerDims& d);
 size_t stream_partial_bytes(const LayerDims& d, int sms);
 bool stream_applies(const LayerDims& d, const Workspace& ws, int sms);
+// T = X . A and bf16(s*T) for at most kStreamMaxTokens tokens (lora_xa_small.cu).
+cudaError_t launch_xa_small(const LayerDims& d, const uint16_t* X, const uint16_t* A, int a_cols, float* XA,
+                            const Workspace& ws, int* status, cudaStream_t stream);
 cudaError_t launch_stream_fwd(const LayerDims& d, const uint16_t* X, const uint8_t* packed, const float* absmax,
                               const uint16_t* B, const Workspace& ws, uint16_t* Y, int* status, int sms,
                               cudaStream_t stream);
@@ -105,18 +128,24 @@ bool make_tensor_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* gadd
 
 // SwiGLU gate of the MLP block (swiglu.cu): h = silu(g) * u from the stacked
 // gate/up output gu [rows, 2*d_ff], and its backward into dgu (same layout).
-cudaError_t launch_swiglu_fwd(const uint16_t* gu, int64_t rows, int64_t d_ff, uint16_t* h, cudaStream_t stream);
-cudaError_t launch_swiglu_bwd(const uint16_t* gu, const uint16_t* dh, int64_t rows, int64_t d_ff, uint16_t* dgu,
+// interleaved: gu's columns in 64-column chunks [gate 0..63 | up 0..63 | gate 64..127 | ...]
+// instead of [gate | up] (d_ff % 64 == 0).
+cudaError_t launch_swiglu_fwd(const uint16_t* gu, int64_t rows, int64_t d_ff, uint16_t* h, bool interleaved,
                               cudaStream_t stream);
+cudaError_t launch_swiglu_bwd(const uint16_t* gu, const uint16_t* dh, int64_t rows, int64_t d_ff, uint16_t* dgu,
+                              bool interleaved, cudaStream_t stream);
 
 // Merged weight bf16(W_deq + s . (A . B)^T) (lora_merge.cu).
 cudaError_t launch_merge_nf4(const uint8_t* packed, const float* absmax, int N, int K, const uint16_t* A,
                              const uint16_t* B, int r, float s, uint16_t* out, int* status,
                              cudaStream_t stream);
 
+// gate_gu / gate_dgu: nullptr, or (for the down layer of a SwiGLU block, K = d_ff)
+// gu [M, 2K] of the forward and dgu [M, 2K] written in place of dX.
 cudaError_t run_backward(const LayerDims& d, const uint16_t* X, const uint16_t* dY,
                          const uint8_t* packed, const float* absmax, const uint16_t* A,
                          const uint16_t* B, const float* XA, uint16_t* dX, float* dA, float* dB,
-                         const Workspace& ws, int* status, cudaStream_t stream);
+                         const Workspace& ws, int* status, cudaStream_t stream,
+                         const uint16_t* gate_gu = nullptr, uint16_t* gate_dgu = nullptr);
 
 }  // namespace qlora

@@ -388,6 +388,11 @@ template <int BN>
 struct MainSmem {
   static constexpr int kStages = main_stages(BN);
   static constexpr int kRaw = raw_stages(BN);
+  // one UMMA of N = BN per K step (at most 256); two TMEM accumulators of BN
+  // columns, so the epilogue of one piece overlaps the main loop of the next
+  static constexpr int kMmaN = BN < 256 ? BN : 256;
+  static constexpr int kHalves = BN / kMmaN;
+  static constexpr int kAccs = 2;
   static constexpr int kActBytes = BN * 128;      // BN tokens x 64 contraction
   static constexpr int kWBytes = kTileP * 128;    // 128 features x 64 contraction
   static constexpr int kStageBytes = kActBytes + kWBytes;
@@ -428,8 +433,19 @@ struct MainParams {
   int dp_rounds;           // ceil(dp_tiles / grid)
   int sk_tiles;            // tiles dp_tiles .. dp_tiles + sk_tiles - 1 are split
   int sk_ctas;             // CTAs sharing the split remainder
+  int debug_stall;         // test hook: the token producer issues nothing, so every wait runs out
+  // SwiGLU gate fused into the epilogue (rows of W and columns of the output
+  // interleaved in 64-row chunks: [gate 0..63 | up 0..63 | gate 64..127 | ...]):
+  //   Y (gate_fwd):  besides gu = the layer's output, h = silu(g) * u via map_h;
+  //   dX (gate_bwd): dh = the layer's dX is not stored; dgu, the gate's backward
+  //                  in the layout of gu, is written from dh and gu.
+  int gate;
+  const uint16_t* gu;      // gate_bwd: [M, 2K] bf16 (the forward's gu)
+  uint16_t* dgu;           // gate_bwd: [M, 2K] bf16
   int* status;
 };
+
+__device__ __forceinline__ float gate_sigmoid(float x) { return 1.f / (1.f + expf(-x)); }
 
 // Piece `idx` of this CTA's work: tile and stage range [sb, se).  Order: the
 // first whole-tile round, then the split pieces, then the other whole-tile
@@ -524,6 +540,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                      const __grid_constant__ CUtensorMap map_out,    // Y or dX, box {64, 32}, 128-B swizzle
                      const __grid_constant__ CUtensorMap map_code,   // packed [N, K/2] bytes; Y box {32, 128}, dX box {64, 64}
                      const __grid_constant__ CUtensorMap map_abs,    // absmax [N, K/64]; Y box {4, 128}, dX box {4, 64}
+                     const __grid_constant__ CUtensorMap map_h,      // gate_fwd: h [M, N/2], box {64, 32}, 128-B swizzle
                      const MainParams p) {
   using S = MainSmem<BN>;
   constexpr int kMainStages = S::kStages;
@@ -580,10 +597,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     tma_prefetch_map(&map_lact);
     tma_prefetch_map(&map_lw);
     tma_prefetch_map(&map_out);
+    if (!kTrans && p.gate) tma_prefetch_map(&map_h);
     tma_prefetch_map(&map_code);
     if (kAbsTma) tma_prefetch_map(&map_abs);
   }
-  if (warp == 1) tmem_alloc(smem_u32(&s_tmem), 2 * BN);
+  if (warp == 1) tmem_alloc(smem_u32(&s_tmem), S::kAccs * BN);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
@@ -591,7 +609,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer for the token operand (and the LoRA stages)
-    if (lane == 0) {
+    // (with debug_stall it loads nothing: no stage completes, the MMA issuer's
+    // bounded wait runs out and records a timeout, every role winds down, and
+    // no copy or MMA is in flight when the CTA exits)
+    if (lane == 0 && !p.debug_stall) {
       int g = 0;
       bool lora_ready = false, stop = false;
       int tile, sb, se;
@@ -607,7 +628,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           const uint32_t act = base + slot * S::kStageBytes;
           if (s < p.num_kt) {
             mbar_arrive_expect_tx(full(slot), S::kActBytes);
-            tma_load_2d(act, &map_act, full(slot), s * kTileK, t0);
+#pragma unroll
+            for (int h = 0; h < S::kHalves; ++h)
+              tma_load_2d(act + h * (S::kMmaN * 128), &map_act, full(slot), s * kTileK, t0 + h * S::kMmaN);
           } else {
             if (!lora_ready) {
               // the low-rank activations come from the previous kernel: wait for it
@@ -619,7 +642,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             }
             const int j = s - p.num_kt;
             mbar_arrive_expect_tx(full(slot), S::kActBytes + S::kWBytes);
-            tma_load_2d(act, &map_lact, full(slot), j * kTileK, t0);
+#pragma unroll
+            for (int h = 0; h < S::kHalves; ++h)
+              tma_load_2d(act + h * (S::kMmaN * 128), &map_lact, full(slot), j * kTileK, t0 + h * S::kMmaN);
             if (kTrans) {
               // A [K, r] rows p0..p0+127, LoRA columns 64j..: K-major
               tma_load_2d(act + S::kActBytes, &map_lw, full(slot), j * kTileK, p0);
@@ -674,8 +699,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     // ---------------- MMA issuer
     if (lane == 0) {
       // A operand majorness: Y -- W tile K-major, B tile MN-major; dX -- W tile MN-major, A tile K-major
-      constexpr uint32_t idesc_w = umma_idesc_bf16(kTileP, BN, kTrans ? 1 : 0, 0);
-      constexpr uint32_t idesc_l = umma_idesc_bf16(kTileP, BN, kTrans ? 0 : 1, 0);
+      constexpr uint32_t idesc_w = umma_idesc_bf16(kTileP, S::kMmaN, kTrans ? 1 : 0, 0);
+      constexpr uint32_t idesc_l = umma_idesc_bf16(kTileP, S::kMmaN, kTrans ? 0 : 1, 0);
       // descriptors: fixed fields once, the start address (16-byte units) added per MMA
       const uint64_t a_hi_k = sw128_desc(0, 16, 1024), a_hi_mn = sw128_desc(0, 8192, 1024);
       const uint64_t b_hi = sw128_desc(0, 16, 1024);
@@ -686,20 +711,26 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const uint64_t a_hi = a_mn ? a_hi_mn : a_hi_k;
         const uint32_t a_step = a_mn ? (2048u >> 4) : (32u >> 4);
         const uint32_t idesc = lora ? idesc_l : idesc_w;
-        const uint32_t b0 = base16 + static_cast<uint32_t>(slot) * (S::kStageBytes >> 4);
-        const uint32_t a0 = b0 + (S::kActBytes >> 4);
-        umma_bf16(tmem_d, a_hi | a0, b_hi | b0, idesc, first ? 0u : 1u);
-        umma_bf16(tmem_d, a_hi | (a0 + a_step), b_hi | (b0 + 2u), idesc, 1u);
-        umma_bf16(tmem_d, a_hi | (a0 + 2u * a_step), b_hi | (b0 + 4u), idesc, 1u);
-        umma_bf16(tmem_d, a_hi | (a0 + 3u * a_step), b_hi | (b0 + 6u), idesc, 1u);
+        const uint32_t bs = base16 + static_cast<uint32_t>(slot) * (S::kStageBytes >> 4);
+        const uint32_t a0 = bs + (S::kActBytes >> 4);
+#pragma unroll
+        for (int h = 0; h < S::kHalves; ++h) {
+          // token half h (rows h*256..) into accumulator columns h*256..
+          const uint32_t b0 = bs + static_cast<uint32_t>(h * S::kMmaN * 128 / 16);
+          const uint32_t d = tmem_d + static_cast<uint32_t>(h * S::kMmaN);
+          umma_bf16(d, a_hi | a0, b_hi | b0, idesc, first ? 0u : 1u);
+          umma_bf16(d, a_hi | (a0 + a_step), b_hi | (b0 + 2u), idesc, 1u);
+          umma_bf16(d, a_hi | (a0 + 2u * a_step), b_hi | (b0 + 4u), idesc, 1u);
+          umma_bf16(d, a_hi | (a0 + 3u * a_step), b_hi | (b0 + 6u), idesc, 1u);
+        }
       };
       int g = 0;
       bool ok = true;
       int tile, sb, se;
       for (int idx = 0; ok && main_piece(p, cta, grid, idx, tile, sb, se); ++idx) {
-        const int acc = idx & 1;
+        const int acc = idx % S::kAccs;
         const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(acc * BN);
-        if (!mbar_wait(tmem_empty(acc), ((idx >> 1) & 1) ^ 1, ab)) break;
+        if (!mbar_wait(tmem_empty(acc), ((idx / S::kAccs) & 1) ^ 1, ab)) break;
         tc_fence_after_sync();
         int s = sb;
         while (s < se) {
@@ -826,6 +857,39 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     const bool odd = (lane & 1) != 0;
     // one chunk of 32 tokens x 128 features (this thread: feature prow) -> bf16 -> Y / dX
     auto store_chunk = [&](const float (&f)[32], int p0, int t0, int c0) {
+      if (kTrans && p.gate) {
+        // dX of the down layer of a SwiGLU block: dh never goes to memory; the
+        // gate's backward turns it, with g and u from gu, into dgu (layout of gu).
+        // dh is rounded to bf16 first, as the unfused block stores it.
+        const int n = p0 + prow;   // a feature of d_ff
+        if (n >= p.K) return;
+        const int64_t pitch = 2 * static_cast<int64_t>(p.K);
+        const int64_t gcol = static_cast<int64_t>(n >> 6) * 128 + (n & 63);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float gv[16], uv[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const int tok = t0 + c0 + 16 * half + q;
+            const int64_t at = static_cast<int64_t>(tok < p.M ? tok : 0) * pitch + gcol;
+            gv[q] = __bfloat162float(__ushort_as_bfloat16(__ldg(p.gu + at)));
+            uv[q] = __bfloat162float(__ushort_as_bfloat16(__ldg(p.gu + at + 64)));
+          }
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const int tok = t0 + c0 + 16 * half + q;
+            if (tok >= p.M) continue;
+            const float dh = __bfloat162float(__float2bfloat16_rn(f[16 * half + q]));
+            const float sg = gate_sigmoid(gv[q]);
+            const float du = dh * gv[q] * sg;
+            const float dg = dh * uv[q] * sg * (1.f + gv[q] * (1.f - sg));
+            const int64_t at = static_cast<int64_t>(tok) * pitch + gcol;
+            p.dgu[at] = __bfloat16_as_ushort(__float2bfloat16_rn(dg));
+            p.dgu[at + 64] = __bfloat16_as_ushort(__float2bfloat16_rn(du));
+          }
+        }
+        return;
+      }
       // the previous chunk's store must have read the staging buffer
       if (leader) tma_store_wait_read_all();
       named_bar_sync(1, 128);
@@ -848,14 +912,47 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         if (p0 + 64 < (kTrans ? p.K : p.N)) tma_store_2d(&map_out, staging + 4096, p0 + 64, t0 + c0);
         tma_store_commit();
       }
+      if (!kTrans && p.gate) {
+        // Y of the gate/up layer of a SwiGLU block: the staging holds the chunk's
+        // gate features (half 0) and the matching up features (half 1), rounded
+        // to bf16 as gu stores them; h = silu(g) * u for token a, features
+        // 16q .. 16q+15 of the 64, then h through the staging's first half.
+        const int et = (warp - 10) * 32 + lane;   // 0..127
+        const uint32_t a = static_cast<uint32_t>(et >> 2), q = static_cast<uint32_t>(et & 3);
+        uint32_t hw[2][4];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const uint32_t off = a * 128u + (((2u * q + k) ^ (a & 7u)) << 4);
+          const uint4 g4v = ld_shared_v4(staging + off), u4v = ld_shared_v4(staging + 4096 + off);
+          const uint32_t gw[4] = {g4v.x, g4v.y, g4v.z, g4v.w}, uw[4] = {u4v.x, u4v.y, u4v.z, u4v.w};
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const float g0 = __uint_as_float(gw[w] << 16), g1 = __uint_as_float(gw[w] & 0xFFFF0000u);
+            const float u0 = __uint_as_float(uw[w] << 16), u1 = __uint_as_float(uw[w] & 0xFFFF0000u);
+            hw[k][w] = pack_bf16x2(g0 * gate_sigmoid(g0) * u0, g1 * gate_sigmoid(g1) * u1);
+          }
+        }
+        if (leader) tma_store_wait_read_all();   // the gu stores have read the staging
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          st_shared_v4(staging + a * 128u + (((2u * q + k) ^ (a & 7u)) << 4),
+                       make_uint4(hw[k][0], hw[k][1], hw[k][2], hw[k][3]));
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (leader && t0 + c0 < p.M) {
+          tma_store_2d(&map_h, staging, p0 >> 1, t0 + c0);
+          tma_store_commit();
+        }
+      }
     };
     int tile, sb, se;
     for (int idx = 0; main_piece(p, cta, grid, idx, tile, sb, se); ++idx) {
       const int p0 = (tile % p.p_tiles) * kTileP;
       const int t0 = (tile / p.p_tiles) * BN;
-      const int acc = idx & 1;
+      const int acc = idx % S::kAccs;
       const uint32_t tacc = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      if (!__all_sync(0xffffffffu, mbar_wait(tmem_full(acc), (idx >> 1) & 1, ab))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(tmem_full(acc), (idx / S::kAccs) & 1, ab))) break;
       tc_fence_after_sync();
       if (sb == 0 && se == total) {
         // a whole tile: straight to the output
@@ -925,7 +1022,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, 2 * BN);
+    tmem_dealloc(tmem_base, S::kAccs * BN);
   }
 }
 
@@ -1088,7 +1185,7 @@ int plan_schedule(int tiles, int total, int bn, const SplitBuffers& sb, MainPara
 }
 
 template <int BN, bool kTrans, bool kAbsTma>
-cudaError_t launch_main_bn(const CUtensorMap (&maps)[6], MainParams mp, int P, int M, const SplitBuffers& sb,
+cudaError_t launch_main_bn(const CUtensorMap (&maps)[7], MainParams mp, int P, int M, const SplitBuffers& sb,
                            cudaStream_t stream) {
   auto kern = lora_main_kernel<BN, kTrans, kAbsTma>;
   cudaError_t e = set_smem(kern, MainSmem<BN>::kBytes);
@@ -1109,11 +1206,11 @@ cudaError_t launch_main_bn(const CUtensorMap (&maps)[6], MainParams mp, int P, i
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   LaunchScope scope(kTrans ? kKindMainDx : kKindMainFwd, stream);
-  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], mp);
+  return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], mp);
 }
 
 template <int BN, bool kTrans>
-cudaError_t launch_main_abs(const CUtensorMap (&maps)[6], const MainParams& mp, bool abs_tma, int P,
+cudaError_t launch_main_abs(const CUtensorMap (&maps)[7], const MainParams& mp, bool abs_tma, int P,
                             int M, const SplitBuffers& sb, cudaStream_t stream) {
   if (abs_tma) return launch_main_bn<BN, kTrans, true>(maps, mp, P, M, sb, stream);
   return launch_main_bn<BN, kTrans, false>(maps, mp, P, M, sb, stream);
@@ -1139,13 +1236,17 @@ LowRankA low_rank_a(const LayerDims& d, const uint16_t* A, const Workspace& ws) 
 template <bool kTrans>
 cudaError_t launch_main(const LayerDims& d, const uint16_t* act, const uint16_t* lact,
                         const uint16_t* lw, int lw_cols, uint16_t* out, const uint8_t* packed,
-                        const float* absmax, const Workspace& ws, int* status, cudaStream_t stream) {
+                        const float* absmax, const Workspace& ws, int* status, cudaStream_t stream,
+                        const GateIo& gate = GateIo{}) {
   const int P = kTrans ? d.K : d.N;     // output features
   const int C = kTrans ? d.N : d.K;     // contraction length of the NF4 part
   const int bn = pick_bn(d.M);
   const bool abs_tma = (d.K % 256) == 0;   // absmax rows are 16-byte multiples
-  CUtensorMap maps[6];
-  bool ok = map_bf16(&maps[0], act, C, d.M, 64, bn, true) && map_bf16(&maps[1], lact, d.rp, d.M, 64, bn, true) &&
+  CUtensorMap maps[7];
+  const bool gated = kTrans ? gate.dgu != nullptr : gate.h != nullptr;
+  if (kTrans && gated) out = gate.dgu;   // dX is not stored; its map is never used
+  const int box_t = bn < 256 ? bn : 256;   // token rows per TMA box
+  bool ok = map_bf16(&maps[0], act, C, d.M, 64, box_t, true) && map_bf16(&maps[1], lact, d.rp, d.M, 64, box_t, true) &&
             make_map(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, P, d.M, static_cast<uint64_t>(P) * 2, 64,
                      kEpiChunk, true);
   if (kTrans) ok = ok && map_bf16(&maps[2], lw, lw_cols, d.K, 64, kTileP, true);   // A [K, r]
@@ -1159,14 +1260,23 @@ cudaError_t launch_main(const LayerDims& d, const uint16_t* act, const uint16_t*
                            kTrans ? 64 : kTileP, CU_TENSOR_MAP_SWIZZLE_NONE);
   else
     maps[5] = maps[4];
+  if (!kTrans && gated)   // h [M, N/2]
+    ok = ok && make_map(&maps[6], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, gate.h, d.N / 2, d.M,
+                        static_cast<uint64_t>(d.N / 2) * 2, 64, kEpiChunk, true);
+  else
+    maps[6] = maps[3];
   if (!ok) return cudaErrorInvalidValue;
   MainParams mp;
+  mp.gate = gated ? 1 : 0;
+  mp.gu = gate.gu;
+  mp.dgu = gate.dgu;
   mp.absmax = absmax;
   mp.M = d.M;
   mp.K = d.K;
   mp.N = d.N;
   mp.num_kt = (C + kTileK - 1) / kTileK;
   mp.num_lt = d.rp / kTileK;
+  mp.debug_stall = take_debug_stall() ? 1 : 0;
   mp.status = status;
   const SplitBuffers sb = {ws.partials, ws.partial_bytes, ws.counters, ws.counter_cap};
   if (bn == 32) return launch_main_abs<32, kTrans>(maps, mp, abs_tma, P, d.M, sb, stream);
@@ -1246,10 +1356,20 @@ Workspace carve_workspace(const LayerDims& d, void* base) {
 
 cudaError_t run_forward(const LayerDims& d, const uint16_t* X, const uint8_t* packed,
                         const float* absmax, const uint16_t* A, const uint16_t* B, uint16_t* Y,
-                        float* XA, const Workspace& ws, int* status, cudaStream_t stream) {
+                        float* XA, const Workspace& ws, int* status, cudaStream_t stream, uint16_t* gate_h) {
   cudaError_t e = launch_pad_a(d, A, ws, stream);
   if (e != cudaSuccess) return e;
   const LowRankA la = low_rank_a(d, A, ws);
+  const int sms = sm_count();
+  if (stream_applies(d, ws, sms)) {
+    // 1..16 tokens: T on one small cluster beside the weight stream
+    e = launch_xa_small(d, X, la.ptr, la.cols, XA, ws, status, stream);
+    if (e == cudaSuccess) e = launch_stream_fwd(d, X, packed, absmax, B, ws, Y, status, sms, stream);
+    // the token-stream kernel's 16-row groups hold gate or up features, never
+    // both: the gate runs as its own pass over the interleaved output
+    if (e == cudaSuccess && gate_h != nullptr) e = launch_swiglu_fwd(Y, d.M, d.N / 2, gate_h, true, stream);
+    return e;
+  }
   // T = X . A  (fp32, saved) and bf16(s*T)
   {
     CUtensorMap maps[4];
@@ -1273,15 +1393,16 @@ cudaError_t run_forward(const LayerDims& d, const uint16_t* X, const uint8_t* pa
     e = launch_skinny<kRowsT>(d.rp, maps, sp, tiles, pick_split(tiles, sp.num_ct), stream);
     if (e != cudaSuccess) return e;
   }
-  const int sms = sm_count();
-  if (stream_applies(d, ws, sms)) return launch_stream_fwd(d, X, packed, absmax, B, ws, Y, status, sms, stream);
-  return launch_main<false>(d, X, ws.s_t, B, d.r, Y, packed, absmax, ws, status, stream);
+  GateIo gate;
+  gate.h = gate_h;
+  return launch_main<false>(d, X, ws.s_t, B, d.r, Y, packed, absmax, ws, status, stream, gate);
 }
 
 cudaError_t run_backward(const LayerDims& d, const uint16_t* X, const uint16_t* dY,
                          const uint8_t* packed, const float* absmax, const uint16_t* A,
                          const uint16_t* B, const float* XA, uint16_t* dX, float* dA, float* dB,
-                         const Workspace& ws, int* status, cudaStream_t stream) {
+                         const Workspace& ws, int* status, cudaStream_t stream, const uint16_t* gate_gu,
+                         uint16_t* gate_dgu) {
   cudaError_t e = launch_pad_a(d, A, ws, stream);
   if (e != cudaSuccess) return e;
   const LowRankA la = low_rank_a(d, A, ws);
@@ -1311,9 +1432,12 @@ cudaError_t run_backward(const LayerDims& d, const uint16_t* X, const uint16_t* 
   }
   // dX first; the dA/dB kernel then runs in the SMs dX's last tiles leave idle.  It may start
   // before dX finishes because dX lets it go only after its own wait on the G kernel.
-  const bool with_dx = dX != nullptr;
+  const bool with_dx = dX != nullptr || gate_dgu != nullptr;
   if (with_dx) {
-    e = launch_main<true>(d, dY, ws.s_g, la.ptr, la.cols, dX, packed, absmax, ws, status, stream);
+    GateIo gate;
+    gate.gu = gate_gu;
+    gate.dgu = gate_dgu;
+    e = launch_main<true>(d, dY, ws.s_g, la.ptr, la.cols, dX, packed, absmax, ws, status, stream, gate);
     if (e != cudaSuccess) return e;
   }
   // dA = X^T . bf16(s*G)  -> [K, r]   and   dB = bf16(s*T)^T . dY  -> [r, N], one launch

@@ -5,18 +5,21 @@
 // 融合与内存优化", section "内核融合"; "这不是“魔法”是把Unsloth的底层优化逻辑榨干了用",
 // section 1), the same result as the main kernel.  With so few tokens the work is
 // 0.5625 bytes of codes and absmax per weight element against 2*M flops, so the
-// kernel is built around keeping enough of the weight in flight to run at the
-// HBM rate, with nothing that makes a warp wait for another:
+// kernel is built around keeping the weight streaming at the HBM rate with as
+// few instructions per element as possible:
 //
-//   * Work item: 32 weight rows (two 16-row MMA groups) x one 64-element NF4
-//     block.  Items are numbered row-pair-major (all blocks of rows 0..31, then
-//     rows 32..63, ...) and every warp of a persistent grid (one CTA per SM)
-//     takes an equal contiguous range of them.
-//   * Each lane loads its quarter of each block row (8 code bytes = 16
-//     elements) for four rows straight into registers with 8-byte loads that
-//     skip L1, several items ahead of the one it computes (a ring of
-//     registers): no shared-memory staging, no barriers.  X comes through L1
-//     with 16-byte loads (every warp of the SM reads the same X).
+//   * Unit: 16 weight rows (one MMA row group) x a slice of up to 1024 input
+//     features (16 NF4 blocks), four items of 256 features.  The CTAs (one per
+//     SM, sixteen warps) are shared out evenly among the slices; each takes
+//     an equal contiguous range of its slice's items, and each warp an equal
+//     contiguous part of its CTA's (at least four items, so a unit has at most
+//     two parts).  The X columns of the CTA's slice are copied into shared
+//     memory once, at the start.
+//   * Each warp streams its own units with its own ring of shared-memory
+//     slots and mbarriers: lane 0 issues 2-D TMA copies of 16 rows x 128 bytes
+//     of codes (256 input features, 128-byte swizzle) and the matching 16 x 4
+//     absmax, four items ahead of the one the warp computes.  No warp waits for
+//     another; the weight arrives in long contiguous DRAM reads.
 //   * Decode: one shared-memory lookup per code byte in a table of the 256
 //     possible bytes -> a pair of bf16 levels, one copy per lane (32 KB, never a
 //     bank conflict), straight into the A registers of mma.sync m16n8k16
@@ -24,25 +27,30 @@
 //     fp32: the sum of bf16(level[q]) * x * absmax, which is the sum of
 //     bf16(level[q] * absmax) * x up to the rounding of the weight (both are
 //     within 2^-9 of level[q] * absmax).
-//   * The contraction order inside an MMA is free: lane (g, t) of the MMA
-//     takes elements 16t .. 16t+15 of the block (its 8 code bytes; k-step s
-//     uses bytes 2s and 2s+1), and the X fragments are read in that order.
-//   * Where a warp's range crosses into the next row pair it writes the
-//     finished segment's fp32 partial to its own slot in the workspace.  After
-//     its range, the warp counts its segments in per-row-pair counters; the
-//     warp that completes a row pair's count adds the pair's partials in warp
-//     order (so results do not depend on timing), adds the low-rank term
-//     bf16(s*T) . B with mma.sync, and stores the 32 rows of Y.
-//   * bf16(s*T) and the zeroed counters come from the rank-r kernel launched
-//     before this one; this kernel is launched with programmatic serialisation
-//     and waits for that kernel (griddepcontrol.wait) only after its stream.
+//   * The contraction order inside an MMA is free: lane (g, t) of the MMA takes
+//     elements 16t .. 16t+15 of a block (its 8 code bytes; k-step s uses bytes
+//     2s and 2s+1), and the X fragments are read in that order.
+//   * Each part of a unit writes its fp32 partial to its own slot (part 0: the
+//     one holding the unit's first item, whose warp also records whether the
+//     unit has a second part).  A second kernel, launched right behind with
+//     programmatic serialisation, gives each 16-row group to one warp: it adds
+//     the group's parts in slice and part order (so the sum does not depend on
+//     timing), adds the low-rank term bf16(s*T) . B with mma.sync, and stores
+//     the 16 rows of Y.  Its CTA brings its 128 columns of B into shared
+//     memory with coalesced loads before it waits for the stream kernel, so
+//     that read overlaps the stream's tail.  There are no atomics and no
+//     counters.
+//   * T comes from the rank-r kernel launched before the stream, which runs
+//     beside it; the stream kernel is launched with programmatic serialisation,
+//     leaves that kernel's SMs free, and waits for it (griddepcontrol.wait)
+//     only at its end, so that the finishing kernel behind it finds T complete.
 //
-// No wait in this kernel depends on another CTA: the reduction is by atomic
-// counters and the last warp to arrive, so there is nothing that can hang.
+// Every mbarrier wait is bounded (kWaitLimitNs): on expiry the CTA records a
+// timeout in the status word and winds down, with no copy left in flight.
 
 #include <cuda_bf16.h>
-#include <cstdint>
 #include <algorithm>
+#include <cstdint>
 #include <cstring>
 
 #include "kernels.h"
@@ -52,12 +60,16 @@
 namespace qlora {
 namespace {
 
-constexpr int kWarps = 16;                   // warps per CTA (one CTA per SM)
+constexpr int kWarps = 16;                    // warps per CTA (one CTA per SM)
 constexpr int kThreads = kWarps * 32;
-constexpr int kPairRows = 32;                // weight rows per item
-constexpr int kRing = 4;                     // items whose codes are in flight per warp
-constexpr int kLutWords = 256 * 32;          // 256 code bytes x 32 lane copies
-constexpr int kMinItemsPerWarp = 4;
+constexpr int kGroupRows = 16;                // weight rows per unit (one MMA row group)
+constexpr int kItemBlocks = 4;                // NF4 blocks per item (one 128-byte code row)
+constexpr int kSliceBlocks = 16;              // NF4 blocks per unit (1024 input features)
+constexpr int kDepth = 4;                     // items in flight per warp
+constexpr int kCodeSlot = kGroupRows * 128;   // bytes of codes per item
+constexpr int kAbsSlot = kGroupRows * 16;     // bytes of absmax per item
+constexpr int kLutWords = 256 * 32;           // 256 code bytes x 32 lane copies
+constexpr int kXPitch = kSliceBlocks * 64 * 2 + 16;   // bytes per token row of a staged X slice
 
 // bf16 bit patterns (round to nearest even) of the NF4 levels, in code order:
 // the host copy kNF4LevelsHost rounded; launch_stream_fwd checks the two agree.
@@ -66,20 +78,35 @@ constexpr uint16_t kLevelBf16[16] = {0xBF80, 0xBF32, 0xBF06, 0xBECA, 0xBE92, 0xB
 __constant__ uint16_t c_level_bf16[16] = {0xBF80, 0xBF32, 0xBF06, 0xBECA, 0xBE92, 0xBE3D, 0xBDBA, 0x0000,
                                           0x3DA3, 0x3E25, 0x3E7C, 0x3EAD, 0x3EE2, 0x3F10, 0x3F39, 0x3F80};
 
+// Shared memory (from a 1024-aligned base, for the swizzled code slots).
+template <int MT>
+struct StreamSmem {
+  static constexpr int kXRows = 8 * MT;
+  static constexpr int kCodeOff = 0;
+  static constexpr int kAbsOff = kCodeOff + kWarps * kDepth * kCodeSlot;
+  static constexpr int kLutOff = kAbsOff + kWarps * kDepth * kAbsSlot;
+  static constexpr int kXOff = kLutOff + kLutWords * 4;
+  static constexpr int kBarOff = kXOff + kXRows * kXPitch;
+  static constexpr int kBytes = kBarOff + 8 * (kWarps * kDepth + 1) + 1024;
+  static_assert(kCodeSlot % 1024 == 0, "code slots keep the 128-byte swizzle alignment");
+  static_assert(kXOff % 16 == 0 && kXPitch % 16 == 0, "bulk copies need 16-byte alignment");
+  static_assert(kBytes <= 227 * 1024, "fits the shared memory of one CTA");
+};
+
 struct StreamParams {
   const uint16_t* X;        // [M, K] bf16
-  const uint8_t* codes;     // [N, K/2]
-  const float* absmax;      // [N, K/64]
   const uint16_t* B;        // [r, N] bf16
   const uint16_t* s_t;      // [M, rp] bf16(s*T), zero columns r..rp-1
   uint16_t* Y;              // [M, N] bf16
-  float* partials;          // slots of 256 * MT floats, slot = global warp + row pair
-  int* counters;            // [row pairs], zero at launch
+  float* partials;          // two slots (parts) of 128 * MT floats per unit
+  int* unit_parts;          // [units]: 1 or 2, written each call by the warp holding part 0
+  int* status;
   int M, K, N, r, rp;
   int kb;                   // NF4 blocks per row: K / 64
-  int pairs;                // row pairs: ceil(N / 32)
-  long long items;          // pairs * kb
-  long long warps;          // warps with work: min(items, warps of the grid); each takes >= 1 item
+  int groups;               // 16-row groups: ceil(N / 16)
+  int slices;               // ceil(kb / 16)
+  int units;                // slices * groups
+  int cps;                  // CTAs per slice
 };
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -88,18 +115,9 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   return v;
 }
 
-// 8 bytes of codes, streamed once: no L1 allocation.
-__device__ __forceinline__ uint2 ldg_stream_v2(const void* p) {
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
   uint2 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ uint4 ldg_v4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
 }
 
@@ -118,43 +136,64 @@ __device__ __forceinline__ uint32_t lut_pair(uint32_t lut_lane, uint32_t w, uint
   return lds32(prmt(w, 0u, sel) * 128u + lut_lane);
 }
 
-// One item's weight loads: rows g, g+8, g+16, g+24 of the pair (g = lane / 4),
-// bytes 8t .. 8t+7 of the block (t = lane % 4), and the four rows' absmax.
-struct ItemLoad {
-  uint2 code[4];
-  float am[4];
+// Blocks of slice s.
+__device__ __forceinline__ int slice_blocks(const StreamParams& p, int s) {
+  return min(kSliceBlocks, p.kb - s * kSliceBlocks);
+}
+
+// Items of unit u.
+__device__ __forceinline__ int unit_items(const StreamParams& p, int u) {
+  return slice_blocks(p, u / p.groups) / kItemBlocks;
+}
+
+// A position in a slice's item list: unit u, item `it` of the unit.
+struct ItemCursor {
+  int u, it;
+  __device__ __forceinline__ void set(const StreamParams& p, int s, int i) {
+    const int ipu = slice_blocks(p, s) / kItemBlocks;
+    u = s * p.groups + i / ipu;
+    it = i % ipu;
+  }
+  __device__ __forceinline__ void next(const StreamParams& p) {
+    if (++it == unit_items(p, u)) {
+      it = 0;
+      ++u;
+    }
+  }
 };
 
-__device__ __forceinline__ void load_item(ItemLoad& it, const StreamParams& p, int pair, int b, int g4, int t) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const int n = pair * kPairRows + g4 + 8 * q;
-    const int nc = n < p.N ? n : p.N - 1;   // rows past the weight: any row, weight 0 below
-    it.code[q] = ldg_stream_v2(p.codes + static_cast<int64_t>(nc) * (p.K >> 1) + b * 32 + t * 8);
-    const float a = ldg_nc_f32(p.absmax + static_cast<int64_t>(nc) * p.kb + b);
-    it.am[q] = n < p.N ? a : 0.0f;
+// The static split of slice s's items: CTA `sub` of the slice takes items
+// [n*sub/cps, n*(sub+1)/cps), and its `active` warps equal parts of those.
+struct SliceSplit {
+  int n;        // items of the slice
+  __device__ __forceinline__ int cta_begin(const StreamParams& p, int sub) const {
+    return static_cast<int>(static_cast<int64_t>(n) * sub / p.cps);
   }
-}
+  __device__ __forceinline__ static int active_warps(int n_cta) { return min(kWarps, max(1, n_cta / kItemBlocks)); }
+};
 
-// X fragments of block b: token half j (tokens 8j + g), elements 16t .. 16t+15.
+// One item's MMAs: acc += absmax * (codes of 16 rows x 4 blocks) . X.
 template <int MT>
-__device__ __forceinline__ void load_x(uint4 (&x)[MT][2], const StreamParams& p, int b, int g4, int t) {
+__device__ __forceinline__ void compute_item(uint32_t code_slot, uint32_t abs_slot, uint32_t x_row0, int blk0,
+                                             uint32_t lut_lane, int g4, int t, float (&acc)[MT][4]) {
 #pragma unroll
-  for (int j = 0; j < MT; ++j) {
-    const int tok = min(8 * j + g4, p.M - 1);   // tokens past M: any row; their outputs are never stored
-    const uint16_t* src = p.X + static_cast<int64_t>(tok) * p.K + b * 64 + t * 16;
-    x[j][0] = ldg_v4(src);
-    x[j][1] = ldg_v4(src + 8);
-  }
-}
-
-// acc[h] += absmax * (this item's MMA sum) for the two 16-row groups h.
-template <int MT>
-__device__ __forceinline__ void compute_item(const ItemLoad& it, const uint4 (&x)[MT][2], uint32_t lut_lane,
-                                             float (&acc)[2][MT][4]) {
+  for (int blk = 0; blk < kItemBlocks; ++blk) {
+    // rows g and g+8, bytes 8t .. 8t+7 of block blk: 16-byte chunk 2*blk + t/2,
+    // swizzled by the row (128-byte swizzle), half t%2 of it
+    const uint32_t chunk = static_cast<uint32_t>(2 * blk + (t >> 1));
+    const uint32_t ra = static_cast<uint32_t>(g4), rb = static_cast<uint32_t>(g4 + 8);
+    const uint2 ca = lds64(code_slot + ra * 128u + ((chunk ^ (ra & 7u)) << 4) + 8u * (t & 1));
+    const uint2 cb = lds64(code_slot + rb * 128u + ((chunk ^ (rb & 7u)) << 4) + 8u * (t & 1));
+    const float am_a = ld_shared_f32(abs_slot + ra * 16u + blk * 4u);
+    const float am_b = ld_shared_f32(abs_slot + rb * 16u + blk * 4u);
+    uint4 x[MT][2];
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const uint2 ca = it.code[2 * h], cb = it.code[2 * h + 1];   // rows g (+16h) and g+8 (+16h)
+    for (int j = 0; j < MT; ++j) {
+      const uint32_t src = x_row0 + static_cast<uint32_t>(j * 8 * kXPitch) +
+                           static_cast<uint32_t>(((blk0 + blk) * 64 + 16 * t) * 2);
+      x[j][0] = ld_shared_v4(src);
+      x[j][1] = ld_shared_v4(src + 16);
+    }
     float d[MT][4];
 #pragma unroll
     for (int j = 0; j < MT; ++j) d[j][0] = d[j][1] = d[j][2] = d[j][3] = 0.0f;
@@ -175,212 +214,250 @@ __device__ __forceinline__ void compute_item(const ItemLoad& it, const uint4 (&x
     }
 #pragma unroll
     for (int j = 0; j < MT; ++j) {
-      acc[h][j][0] = fmaf(it.am[2 * h], d[j][0], acc[h][j][0]);
-      acc[h][j][1] = fmaf(it.am[2 * h], d[j][1], acc[h][j][1]);
-      acc[h][j][2] = fmaf(it.am[2 * h + 1], d[j][2], acc[h][j][2]);
-      acc[h][j][3] = fmaf(it.am[2 * h + 1], d[j][3], acc[h][j][3]);
+      acc[j][0] = fmaf(am_a, d[j][0], acc[j][0]);
+      acc[j][1] = fmaf(am_a, d[j][1], acc[j][1]);
+      acc[j][2] = fmaf(am_b, d[j][2], acc[j][2]);
+      acc[j][3] = fmaf(am_b, d[j][3], acc[j][3]);
     }
   }
 }
 
-// The warp whose range holds item x (ranges are [items*w/W, items*(w+1)/W)).
-__device__ __forceinline__ long long owner_warp(long long x, long long items, long long W) {
-  return ((x + 1) * W - 1) / items;
+template <int MT>
+__device__ __forceinline__ float* slot_ptr(const StreamParams& p, int unit, int part, int lane) {
+  return p.partials + (static_cast<int64_t>(unit) * 2 + part) * (128 * MT) + lane * 4;
 }
 
-template <int MT>
-__device__ __forceinline__ float* slot_ptr(const StreamParams& p, long long slot, int lane) {
-  return p.partials + slot * (256 * MT) + lane * 4;
-}
+constexpr int kFinWarps = 8;                      // 16-row groups per finishing CTA
+constexpr int kFinCols = kFinWarps * kGroupRows;   // columns of B per finishing CTA
+constexpr int kFinBPitch = kFinCols * 2 + 16;      // bytes per rank row of the staged B tile
 
-template <int MT>
-__device__ __forceinline__ void store_partial(const StreamParams& p, long long slot, int lane,
-                                              const float (&acc)[2][MT][4]) {
-  float* dst = slot_ptr<MT>(p, slot, lane);
-#pragma unroll
-  for (int h = 0; h < 2; ++h)
-#pragma unroll
-    for (int j = 0; j < MT; ++j)
-      __stcg(reinterpret_cast<float4*>(dst + (h * MT + j) * 128),
-             make_float4(acc[h][j][0], acc[h][j][1], acc[h][j][2], acc[h][j][3]));
-}
-
-// Finishes row pair `pair`: its partials in warp order, the low-rank term, Y.
-template <int MT>
-__device__ __forceinline__ void finish_pair(const StreamParams& p, int pair, long long W, int lane) {
+// Finishes row group `group` (warp `gw` of its CTA): its units' sums in slice
+// and part order, the low-rank term with B from the CTA's tile (b_tile: rp rows
+// of kFinCols columns) and bf16(s*T) from s_t (16 rows of rp), then Y.
+template <int MT, int RP>
+__device__ __forceinline__ void finish_group(const StreamParams& p, int group, int gw, int lane, uint32_t b_tile,
+                                             uint32_t s_t) {
   const int g4 = lane >> 2, t = lane & 3;
-  const long long first = owner_warp(static_cast<long long>(pair) * p.kb, p.items, W);
-  const long long last = owner_warp(static_cast<long long>(pair) * p.kb + p.kb - 1, p.items, W);
-  float acc[2][MT][4];
-  {
-    const float* src = slot_ptr<MT>(p, first + pair, lane);
+  const int na = group * kGroupRows + g4, nb = na + 8;
+  float acc[MT][4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+  for (int j = 0; j < MT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+  // both parts' slots are read together with the part count; a second part
+  // that was not written this call is ignored (never added)
+#pragma unroll 4
+  for (int s = 0; s < p.slices; ++s) {
+    const int uid = s * p.groups + group;
+    const int parts = __ldcg(p.unit_parts + uid);
+    const float* src0 = slot_ptr<MT>(p, uid, 0, lane);
+    const float* src1 = slot_ptr<MT>(p, uid, 1, lane);
 #pragma unroll
-      for (int j = 0; j < MT; ++j) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (h * MT + j) * 128));
-        acc[h][j][0] = v.x;
-        acc[h][j][1] = v.y;
-        acc[h][j][2] = v.z;
-        acc[h][j][3] = v.w;
-      }
-  }
-  for (long long w = first + 1; w <= last; ++w) {
-    const float* src = slot_ptr<MT>(p, w + pair, lane);
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int j = 0; j < MT; ++j) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(src + (h * MT + j) * 128));
-        acc[h][j][0] += v.x;
-        acc[h][j][1] += v.y;
-        acc[h][j][2] += v.z;
-        acc[h][j][3] += v.w;
-      }
+    for (int j = 0; j < MT; ++j) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(src0 + j * 128));
+      const float4 w = __ldcg(reinterpret_cast<const float4*>(src1 + j * 128));
+      const bool two = parts == 2;
+      acc[j][0] += two ? v.x + w.x : v.x;
+      acc[j][1] += two ? v.y + w.y : v.y;
+      acc[j][2] += two ? v.z + w.z : v.z;
+      acc[j][3] += two ? v.w + w.w : v.w;
+    }
   }
   // low-rank term: D += B^T (rows n, columns j) . bf16(s*T)^T (rows j, columns tokens)
-  const uint16_t* Bp = p.B;
-  for (int j0 = 0; j0 < p.rp; j0 += 16) {
-    uint32_t bt[MT][2];
+  const uint32_t col = static_cast<uint32_t>(gw * kGroupRows + g4) * 2u;   // column g of the group in the tile
+#pragma unroll
+  for (int ks = 0; ks < RP / 16; ++ks) {
+    const uint32_t r0 = b_tile + static_cast<uint32_t>(16 * ks + 2 * t) * kFinBPitch + col;
+    auto u16 = [](uint32_t addr) -> uint32_t {
+      uint16_t v;
+      asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+      return v;
+    };
+    const uint32_t a[4] = {u16(r0) | (u16(r0 + kFinBPitch) << 16), u16(r0 + 16) | (u16(r0 + kFinBPitch + 16) << 16),
+                           u16(r0 + 8 * kFinBPitch) | (u16(r0 + 9 * kFinBPitch) << 16),
+                           u16(r0 + 8 * kFinBPitch + 16) | (u16(r0 + 9 * kFinBPitch + 16) << 16)};
 #pragma unroll
     for (int j = 0; j < MT; ++j) {
-      const int tok = 8 * j + g4;
-      const uint32_t* row = reinterpret_cast<const uint32_t*>(p.s_t + static_cast<int64_t>(tok < p.M ? tok : 0) * p.rp);
-      bt[j][0] = tok < p.M ? __ldcg(row + ((j0 + 2 * t) >> 1)) : 0u;
-      bt[j][1] = tok < p.M ? __ldcg(row + ((j0 + 2 * t + 8) >> 1)) : 0u;
-    }
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int na = pair * kPairRows + 16 * h + g4, nb = na + 8;
-      auto bval = [&](int jj, int n) -> uint32_t {
-        return (jj < p.r && n < p.N) ? static_cast<uint32_t>(__ldg(Bp + static_cast<int64_t>(jj) * p.N + n)) : 0u;
-      };
-      const int ja = j0 + 2 * t;
-      const uint32_t a[4] = {bval(ja, na) | (bval(ja + 1, na) << 16), bval(ja, nb) | (bval(ja + 1, nb) << 16),
-                             bval(ja + 8, na) | (bval(ja + 9, na) << 16), bval(ja + 8, nb) | (bval(ja + 9, nb) << 16)};
-#pragma unroll
-      for (int j = 0; j < MT; ++j) mma_16816(acc[h][j], a, bt[j][0], bt[j][1]);
+      const uint32_t trow = s_t + static_cast<uint32_t>((8 * j + g4) * (RP * 2 + 16) + (16 * ks + 2 * t) * 2);
+      mma_16816(acc[j], a, lds32(trow), lds32(trow + 16));
     }
   }
-  // Y: c0, c1 -> row g (+16h), tokens 2t, 2t+1; c2, c3 -> row g+8
+  // Y: c0, c1 -> row g, tokens 2t, 2t+1 of the half; c2, c3 -> row g+8
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int na = pair * kPairRows + 16 * h + g4, nb = na + 8;
+  for (int j = 0; j < MT; ++j) {
+    const int tok = 8 * j + 2 * t;
 #pragma unroll
-    for (int j = 0; j < MT; ++j) {
-      const int tok = 8 * j + 2 * t;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int n = (e < 2) ? na : nb, tk = tok + (e & 1);
-        if (n < p.N && tk < p.M)
-          p.Y[static_cast<int64_t>(tk) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[h][j][e]));
-      }
+    for (int e = 0; e < 4; ++e) {
+      const int n = (e < 2) ? na : nb, tk = tok + (e & 1);
+      if (n < p.N && tk < p.M)
+        p.Y[static_cast<int64_t>(tk) * p.N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(acc[j][e]));
     }
   }
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kThreads, 1) lora_stream_kernel(const StreamParams p) {
-  __shared__ __align__(16) uint32_t s_lut[kLutWords];
+__global__ void __launch_bounds__(kThreads, 1)
+    lora_stream_kernel(const __grid_constant__ CUtensorMap map_codes,   // [N, K/2] bytes, box {128, 16}, 128-B swizzle
+                       const __grid_constant__ CUtensorMap map_abs,     // [N, K/64] fp32, box {4, 16}
+                       const StreamParams p) {
+  using S = StreamSmem<MT>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_abort;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - smem_u32(smem_raw));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g4 = lane >> 2, t = lane & 3;
+
+  // this CTA's slice and items, and this warp's part of them
+  const int slice = blockIdx.x / p.cps, sub = blockIdx.x % p.cps;
+  const SliceSplit split{p.groups * (slice_blocks(p, slice) / kItemBlocks)};
+  const int i_begin = split.cta_begin(p, sub), i_end = split.cta_begin(p, sub + 1);
+  const int n_cta = i_end - i_begin;
+  const int active = SliceSplit::active_warps(n_cta);   // at least four items per warp
+  const int w_lo = warp < active ? i_begin + n_cta * warp / active : i_end;
+  const int w_hi = warp < active ? i_begin + n_cta * (warp + 1) / active : i_end;
+  const int n_items = w_hi - w_lo;
+  const uint32_t x_bar = base + S::kBarOff + 8u * (kWarps * kDepth);
+  auto full = [&](int slot) { return base + S::kBarOff + 8u * static_cast<uint32_t>(warp * kDepth + slot); };
+  Abort ab{&s_abort, p.status};
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < kWarps * kDepth; ++i) mbar_init(base + S::kBarOff + 8u * i, 1);
+    mbar_init(x_bar, 1);
+    fence_barrier_init();
+  }
   // the decode table: word 32 v + l holds bf16(level[v >> 4]) (the byte's first
   // element) in its low half and bf16(level[v & 15]) in its high half
+  uint32_t* const lut = reinterpret_cast<uint32_t*>(gbase + S::kLutOff);
   for (int i = threadIdx.x; i < kLutWords; i += kThreads) {
     const int v = i >> 5;
-    s_lut[i] = static_cast<uint32_t>(c_level_bf16[v >> 4]) | (static_cast<uint32_t>(c_level_bf16[v & 15]) << 16);
+    lut[i] = static_cast<uint32_t>(c_level_bf16[v >> 4]) | (static_cast<uint32_t>(c_level_bf16[v & 15]) << 16);
+  }
+  // X rows of tokens past M are zero (their MMA columns are never stored)
+  for (int i = threadIdx.x; i < S::kXRows * (kXPitch / 16); i += kThreads) {
+    if (i / (kXPitch / 16) >= p.M) st_shared_v4(base + S::kXOff + static_cast<uint32_t>(i) * 16u, make_uint4(0u, 0u, 0u, 0u));
   }
   __syncthreads();
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g4 = lane >> 2, t = lane & 3;
-  const uint32_t lut_lane = smem_u32(s_lut) + static_cast<uint32_t>(lane) * 4u;
-  const long long W = p.warps;
-  const long long wg = static_cast<long long>(blockIdx.x) * kWarps + warp;
-  const long long lo = wg < W ? p.items * wg / W : 0, hi = wg < W ? p.items * (wg + 1) / W : 0;
-
-  if (lo < hi) {
-    // ring of code loads, kRing items ahead
-    ItemLoad ring[kRing];
-    int lpair = static_cast<int>(lo / p.kb), lb = static_cast<int>(lo % p.kb);   // next item to load
-#pragma unroll
-    for (int u = 0; u < kRing; ++u) {
-      if (lo + u < hi) load_item(ring[u], p, lpair, lb, g4, t);
-      if (++lb == p.kb) {
-        lb = 0;
-        ++lpair;
-      }
-    }
-    int cpair = static_cast<int>(lo / p.kb), cb = static_cast<int>(lo % p.kb);   // item being computed
-    uint4 xn[MT][2];
-    load_x<MT>(xn, p, cb, g4, t);
-    float acc[2][MT][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h)
-#pragma unroll
-      for (int j = 0; j < MT; ++j) acc[h][j][0] = acc[h][j][1] = acc[h][j][2] = acc[h][j][3] = 0.0f;
-
-    for (long long base = lo; base < hi; base += kRing) {
-#pragma unroll
-      for (int u = 0; u < kRing; ++u) {
-        const long long i = base + u;
-        if (i < hi) {
-          uint4 x[MT][2];
-#pragma unroll
-          for (int j = 0; j < MT; ++j) {
-            x[j][0] = xn[j][0];
-            x[j][1] = xn[j][1];
-          }
-          // the next item's X, one item ahead (it is an L1 hit most of the time)
-          const int nb = cb + 1 == p.kb ? 0 : cb + 1;
-          if (i + 1 < hi) load_x<MT>(xn, p, nb, g4, t);
-          compute_item<MT>(ring[u], x, lut_lane, acc);
-          // refill this ring slot kRing items ahead
-          if (i + kRing < hi) load_item(ring[u], p, lpair, lb, g4, t);
-          if (++lb == p.kb) {
-            lb = 0;
-            ++lpair;
-          }
-          // end of a row pair's segment, or of the range: park the partial
-          const bool seg_end = (nb == 0) || (i + 1 == hi);
-          if (seg_end) {
-            store_partial<MT>(p, wg + cpair, lane, acc);
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-              for (int j = 0; j < MT; ++j) acc[h][j][0] = acc[h][j][1] = acc[h][j][2] = acc[h][j][3] = 0.0f;
-          }
-          cb = nb;
-          if (nb == 0) ++cpair;
-        }
-      }
-    }
+  if (threadIdx.x == 0) {
+    // X columns of the CTA's slice, one bulk copy per token row
+    const uint32_t row_bytes = static_cast<uint32_t>(slice_blocks(p, slice) * 128);
+    mbar_arrive_expect_tx(x_bar, row_bytes * static_cast<uint32_t>(p.M));
+    for (int tok = 0; tok < p.M; ++tok)
+      bulk_load_1d(base + S::kXOff + static_cast<uint32_t>(tok * kXPitch),
+                   p.X + static_cast<int64_t>(tok) * p.K + slice * (kSliceBlocks * 64), row_bytes, x_bar);
   }
 
-  // bf16(s*T) and the zeroed counters come from the kernel before this one
+  const uint32_t code_ring = base + S::kCodeOff + static_cast<uint32_t>(warp * kDepth * kCodeSlot);
+  const uint32_t abs_ring = base + S::kAbsOff + static_cast<uint32_t>(warp * kDepth * kAbsSlot);
+  auto issue = [&](const ItemCursor& ic, int slot) {
+    const int g = ic.u % p.groups, s = ic.u / p.groups;
+    const int blk0 = s * kSliceBlocks + ic.it * kItemBlocks;
+    mbar_arrive_expect_tx(full(slot), kCodeSlot + kAbsSlot);
+    tma_load_2d(code_ring + slot * kCodeSlot, &map_codes, full(slot), blk0 * 32, g * kGroupRows);
+    tma_load_2d(abs_ring + slot * kAbsSlot, &map_abs, full(slot), blk0, g * kGroupRows);
+  };
+
+  ItemCursor load_c;
+  load_c.set(p, slice, w_lo);
+  if (lane == 0) {
+    tma_prefetch_map(&map_codes);
+    tma_prefetch_map(&map_abs);
+    ItemCursor ic = load_c;
+    for (int q = 0; q < kDepth && q < n_items; ++q) {
+      issue(ic, q);
+      ic.next(p);
+    }
+  }
+  // every lane acquires the bulk-copied X itself
+  bool ok = mbar_wait_spin(x_bar, 0, ab);
+  const uint32_t lut_lane = base + S::kLutOff + static_cast<uint32_t>(lane) * 4u;
+  float acc[MT][4];
+#pragma unroll
+  for (int j = 0; j < MT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+  ItemCursor cur = load_c;
+  if (lane == 0)
+    for (int q = 0; q < kDepth && q < n_items; ++q) load_c.next(p);   // the lane-0 cursor, kDepth ahead
+  int seg_part = cur.it == 0 ? 0 : 1;   // the current part of a unit
+  int k = 0;
+  for (; ok && k < n_items; ++k) {
+    const int slot = k % kDepth;
+    if (!__all_sync(0xffffffffu, mbar_wait_spin(full(slot), (k / kDepth) & 1, ab))) {
+      ok = false;
+      break;
+    }
+    const uint32_t x_row0 = base + S::kXOff + static_cast<uint32_t>(g4 * kXPitch);
+    compute_item<MT>(code_ring + slot * kCodeSlot, abs_ring + slot * kAbsSlot, x_row0, cur.it * kItemBlocks,
+                     lut_lane, g4, t, acc);
+    // the slot's codes have been read by every lane: refill it kDepth items ahead
+    __syncwarp();
+    if (lane == 0 && k + kDepth < n_items) {
+      fence_proxy_async_smem();
+      issue(load_c, slot);
+      load_c.next(p);
+    }
+    if (cur.it + 1 == unit_items(p, cur.u) || k + 1 == n_items) {
+      // the end of this warp's part of the unit (part 0 records whether it is the whole unit)
+      if (seg_part == 0 && lane == 0) p.unit_parts[cur.u] = cur.it + 1 == unit_items(p, cur.u) ? 1 : 2;
+      float* dst = slot_ptr<MT>(p, cur.u, seg_part, lane);
+#pragma unroll
+      for (int j = 0; j < MT; ++j) {
+        __stcg(reinterpret_cast<float4*>(dst + j * 128), make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]));
+        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+      }
+      seg_part = 0;
+    }
+    cur.next(p);
+  }
+  if (!ok) {
+    // a wait ran out: let the copies this CTA issued land before it exits
+    if (lane == 0)
+      for (int q = k; q < n_items && q < k + kDepth; ++q) mbar_wait_spin(full(q % kDepth), (q / kDepth) & 1, ab, false);
+    if (threadIdx.x == 0) mbar_wait_spin(x_bar, 0, ab, false);
+    return;
+  }
+
+  // the finishing kernel behind this one reads T: this grid completes only
+  // after the rank-r kernel before it has; then let the finishing kernel start
   griddep_wait();
-  if (lo >= hi) return;
-  __threadfence();   // this lane's partial stores, before the warp's counter updates
-  __syncwarp();
-  const int pair_first = static_cast<int>(lo / p.kb), pair_last = static_cast<int>((hi - 1) / p.kb);
-  for (int pair = pair_first; pair <= pair_last; ++pair) {
-    const long long first = owner_warp(static_cast<long long>(pair) * p.kb, p.items, W);
-    const long long last = owner_warp(static_cast<long long>(pair) * p.kb + p.kb - 1, p.items, W);
-    int arrived = 0;
-    if (lane == 0) arrived = atomicAdd(p.counters + pair, 1);
-    arrived = __shfl_sync(0xffffffffu, arrived, 0);
-    if (arrived == static_cast<int>(last - first)) {
-      __threadfence();   // the other warps' partials, after their counter updates
-      finish_pair<MT>(p, pair, W, lane);
-    }
+  griddep_launch_dependents();
+}
+
+// The 16-row groups, one per warp: parts in slice order, the low-rank term, Y.
+template <int MT, int RP>
+__global__ void __launch_bounds__(kFinWarps * 32) lora_stream_finish_kernel(const StreamParams p) {
+  __shared__ __align__(16) uint8_t b_tile[RP * kFinBPitch];          // B [rp][this CTA's 128 columns]
+  __shared__ __align__(16) uint8_t t_tile[16 * (RP * 2 + 16)];       // bf16(s*T) [16 tokens][rp]
+  const int n0 = static_cast<int>(blockIdx.x) * kFinCols;
+  // B is an input of the call: bring this CTA's columns in while the stream kernel finishes
+  for (int i = threadIdx.x; i < RP * (kFinCols / 8); i += kFinWarps * 32) {
+    const int j = i / (kFinCols / 8), c = (i % (kFinCols / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (j < p.r && n0 + c < p.N) v = ldg_nc_v4(p.B + static_cast<int64_t>(j) * p.N + n0 + c);
+    st_shared_v4(smem_u32(b_tile) + static_cast<uint32_t>(j * kFinBPitch + c * 2), v);
   }
+  // the stream kernel before this one wrote the partials (and completed after the rank-r kernel)
+  griddep_wait();
+  for (int i = threadIdx.x; i < 16 * (RP / 8); i += kFinWarps * 32) {
+    const int tok = i / (RP / 8), c = (i % (RP / 8)) * 8;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (tok < p.M) v = *reinterpret_cast<const uint4*>(p.s_t + static_cast<int64_t>(tok) * p.rp + c);
+    st_shared_v4(smem_u32(t_tile) + static_cast<uint32_t>(tok * (RP * 2 + 16) + c * 2), v);
+  }
+  __syncthreads();
+  const int gw = static_cast<int>(threadIdx.x >> 5);
+  const int g = static_cast<int>(blockIdx.x) * kFinWarps + gw;
+  if (g < p.groups) finish_group<MT, RP>(p, g, gw, threadIdx.x & 31, smem_u32(b_tile), smem_u32(t_tile));
 }
 
 template <int MT>
-cudaError_t launch_stream_mt(const StreamParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_stream_mt(const CUtensorMap (&maps)[2], const StreamParams& p, int grid, cudaStream_t stream) {
   auto kern = lora_stream_kernel<MT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, StreamSmem<MT>::kBytes);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = StreamSmem<MT>::kBytes;
   cfg.stream = stream;
   // programmatic serialisation: the weight stream starts while the rank-r
   // kernel before this one finishes; bf16(s*T) and the counters wait for it
@@ -389,32 +466,53 @@ cudaError_t launch_stream_mt(const StreamParams& p, int grid, cudaStream_t strea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  LaunchScope scope(kKindStream, stream);
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  {
+    LaunchScope scope(kKindStream, stream);
+    e = cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], p);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t fin = cfg;
+  fin.gridDim = dim3((p.groups + kFinWarps - 1) / kFinWarps, 1, 1);
+  fin.blockDim = dim3(kFinWarps * 32, 1, 1);
+  fin.dynamicSmemBytes = 0;
+  LaunchScope scope(kKindStreamFinish, stream);
+  if (p.rp == 64) return cudaLaunchKernelEx(&fin, lora_stream_finish_kernel<MT, 64>, p);
+  return cudaLaunchKernelEx(&fin, lora_stream_finish_kernel<MT, 128>, p);
 }
 
-long long stream_items(const LayerDims& d) {
-  return static_cast<long long>((d.N + kPairRows - 1) / kPairRows) * (d.K / 64);
-}
+int stream_groups(const LayerDims& d) { return (d.N + kGroupRows - 1) / kGroupRows; }
 
-int stream_grid(const LayerDims& d, int sms) {
-  const long long want = (stream_items(d) + kWarps * kMinItemsPerWarp - 1) / (kWarps * kMinItemsPerWarp);
-  return static_cast<int>(want < sms ? (want < 1 ? 1 : want) : sms);
+int stream_units(const LayerDims& d) {
+  const int kb = d.K / 64;
+  return ((kb + kSliceBlocks - 1) / kSliceBlocks) * stream_groups(d);
 }
 
 }  // namespace
 
-int stream_counter_slots(const LayerDims& d) { return (d.N + kPairRows - 1) / kPairRows; }
-
-size_t stream_partial_bytes(const LayerDims& d, int sms) {
-  const int mt = d.M <= 8 ? 1 : 2;
-  const long long slots = static_cast<long long>(stream_grid(d, sms)) * kWarps + stream_counter_slots(d);
-  return static_cast<size_t>(slots) * 256 * mt * sizeof(float);
+int stream_counter_slots(const LayerDims& d) {
+  (void)d;
+  return 0;   // the token-stream forward uses no counters
 }
 
+namespace {
+size_t stream_slot_bytes(const LayerDims& d) {
+  const int mt = d.M <= 8 ? 1 : 2;
+  // two slots per unit, then a part count per unit
+  return (static_cast<size_t>(stream_units(d)) * (2 * 128 * mt * sizeof(float) + sizeof(int)) + 15) & ~size_t(15);
+}
+}  // namespace
+
+size_t stream_partial_bytes(const LayerDims& d, int sms) {
+  (void)sms;
+  return stream_slot_bytes(d);
+}
+
+// The absmax rows are read by TMA in 16-byte boxes, and an item is four blocks:
+// K a multiple of 256; and there must be a CTA for every slice.
 bool stream_applies(const LayerDims& d, const Workspace& ws, int sms) {
-  if (d.M < 1 || d.M > kStreamMaxTokens || d.K % 64 != 0) return false;
-  if (ws.counters == nullptr || ws.partials == nullptr || ws.counter_cap < stream_counter_slots(d)) return false;
+  if (d.M < 1 || d.M > kStreamMaxTokens || d.K % 256 != 0) return false;
+  if ((d.K / 64 + kSliceBlocks - 1) / kSliceBlocks > sms - kStreamReservedSms) return false;
+  if (ws.partials == nullptr) return false;
   return ws.partial_bytes >= stream_partial_bytes(d, sms);
 }
 
@@ -432,30 +530,39 @@ bool level_table_matches() {
 cudaError_t launch_stream_fwd(const LayerDims& d, const uint16_t* X, const uint8_t* packed, const float* absmax,
                               const uint16_t* B, const Workspace& ws, uint16_t* Y, int* status, int sms,
                               cudaStream_t stream) {
-  (void)status;   // nothing in this kernel waits, so nothing can time out
   static const bool table_ok = level_table_matches();
   if (!table_ok) return cudaErrorInvalidValue;
+  CUtensorMap maps[2];
+  // codes [N, K/2] bytes: 128-byte rows of 16-row boxes, swizzled; absmax [N, K/64] fp32, 4 blocks x 16 rows
+  bool ok = make_tensor_map_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, packed, d.K / 2, d.N, d.K / 2, 128,
+                               kGroupRows, CU_TENSOR_MAP_SWIZZLE_128B) &&
+            make_tensor_map_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, absmax, d.K / 64, d.N, d.K / 16, 4,
+                               kGroupRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (!ok) return cudaErrorInvalidValue;
   StreamParams p;
   p.X = X;
-  p.codes = packed;
-  p.absmax = absmax;
   p.B = B;
   p.s_t = ws.s_t;
   p.Y = Y;
   p.partials = ws.partials;
-  p.counters = ws.counters;
+  p.unit_parts = reinterpret_cast<int*>(ws.partials + static_cast<size_t>(stream_units(d)) * 2 * 128 * (d.M <= 8 ? 1 : 2));
+  p.status = status;
   p.M = d.M;
   p.K = d.K;
   p.N = d.N;
   p.r = d.r;
   p.rp = d.rp;
   p.kb = d.K / 64;
-  p.pairs = stream_counter_slots(d);
-  p.items = stream_items(d);
-  const int grid = stream_grid(d, sms);
-  p.warps = std::min<long long>(p.items, static_cast<long long>(grid) * kWarps);
-  if (d.M <= 8) return launch_stream_mt<1>(p, grid, stream);
-  return launch_stream_mt<2>(p, grid, stream);
+  p.groups = stream_groups(d);
+  p.slices = (p.kb + kSliceBlocks - 1) / kSliceBlocks;
+  p.units = p.slices * p.groups;
+  // the CTAs are shared out among the slices (at least four items each), and
+  // leave the rank-r kernel's SMs free so that every CTA starts at once beside it
+  const int slice_items = p.groups * (kSliceBlocks / kItemBlocks);
+  p.cps = std::max(1, std::min((sms - kStreamReservedSms) / p.slices, slice_items / kItemBlocks));
+  const int grid = p.slices * p.cps;
+  if (d.M <= 8) return launch_stream_mt<1>(maps, p, grid, stream);
+  return launch_stream_mt<2>(maps, p, grid, stream);
 }
 
 }  // namespace qlora

@@ -95,7 +95,8 @@ std::vector<cudaEvent_t> g_free_events;
 
 const char* const kKindNames[qlora::kNumKernelKinds] = {
     "nf4_quantize", "nf4_dequant", "lora_pad_A", "lora_rows_T", "lora_rows_G",
-    "lora_red_dA_dB", "lora_main_fwd", "lora_main_dX", "lora_merge", "lora_stream_fwd", "swiglu_fwd", "swiglu_bwd"};
+    "lora_red_dA_dB", "lora_main_fwd", "lora_main_dX", "lora_merge", "lora_stream_fwd", "swiglu_fwd", "swiglu_bwd",
+    "lora_stream_finish"};
 
 cudaEvent_t take_event() {
   if (!g_free_events.empty()) {
@@ -113,6 +114,18 @@ cudaEvent_t take_event() {
 namespace qlora {
 
 void record_cuda_error(int cuda_error) { g_last_cuda_error = cuda_error; }
+
+namespace {
+std::atomic<int> g_debug_stall_launches{0};
+}  // namespace
+
+bool take_debug_stall() {
+  int n = g_debug_stall_launches.load(std::memory_order_relaxed);
+  while (n > 0) {
+    if (g_debug_stall_launches.compare_exchange_weak(n, n - 1, std::memory_order_relaxed)) return true;
+  }
+  return false;
+}
 
 int* device_status_word(int* cuda_error) {
   int* word = nullptr;
@@ -176,6 +189,12 @@ int qlora_profile_collect(const char** names, float* total_ms, int* launches, in
 }
 
 int64_t qlora_launch_count(void) { return g_launches.load(); }
+
+qlora_status qlora_debug_stall_main_launches(int launches) {
+  if (launches < 0) return QLORA_ERR_SHAPE;
+  qlora::g_debug_stall_launches.store(launches);
+  return QLORA_OK;
+}
 
 
 const char* qlora_status_string(qlora_status status) {
@@ -271,7 +290,7 @@ qlora_status qlora_swiglu_fwd(const uint16_t* gu, int64_t M, int64_t d_ff, uint1
   if (M == 0) return QLORA_OK;
   if (!gu || !h) return QLORA_ERR_NULL;
   if (!aligned16(gu) || !aligned16(h)) return QLORA_ERR_ALIGN;
-  cudaError_t e = qlora::launch_swiglu_fwd(gu, M, d_ff, h, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = qlora::launch_swiglu_fwd(gu, M, d_ff, h, false, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
 }
 
@@ -282,7 +301,7 @@ qlora_status qlora_swiglu_bwd(const uint16_t* gu, const uint16_t* dh, int64_t M,
   if (M == 0) return QLORA_OK;
   if (!gu || !dh || !dgu) return QLORA_ERR_NULL;
   if (!aligned16(gu) || !aligned16(dh) || !aligned16(dgu)) return QLORA_ERR_ALIGN;
-  cudaError_t e = qlora::launch_swiglu_bwd(gu, dh, M, d_ff, dgu, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = qlora::launch_swiglu_bwd(gu, dh, M, d_ff, dgu, false, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
 }
 
@@ -344,6 +363,120 @@ qlora_status qlora_linear_bwd(const uint16_t* X, const uint16_t* dY, int64_t M, 
   cudaError_t e = qlora::run_backward(d, X, dY, packed, absmax, A, B, XA_saved, dX, dA, dB,
                                       qlora::carve_workspace(d, workspace), status, cs);
   return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------- SwiGLU MLP block, gate fused
+
+qlora_status qlora_linear_fwd_swiglu(const uint16_t* X, int64_t M, int64_t d_in, int64_t d_ff,
+                                     const uint8_t* packed, const float* absmax, const uint16_t* A,
+                                     const uint16_t* B, int32_t r, float s, uint16_t* gu, uint16_t* h,
+                                     float* XA_save, void* workspace, size_t workspace_bytes,
+                                     qlora_stream_t stream) {
+  if (d_ff < 1 || d_ff > kMaxDim / 2) return QLORA_ERR_SHAPE;
+  if (d_ff % 64 != 0) return QLORA_ERR_UNSUPPORTED;
+  const int64_t d_out = 2 * d_ff;
+  qlora_status st = check_layer(M, d_in, d_out, r);
+  if (st != QLORA_OK) return st;
+  if (!packed || !absmax || !A || !B) return QLORA_ERR_NULL;
+  if (M == 0) return QLORA_OK;
+  if (!X || !gu || !h || !XA_save) return QLORA_ERR_NULL;
+  if (!aligned16(X) || !aligned16(packed) || !aligned16(absmax) || !aligned16(A) || !aligned16(B) ||
+      !aligned16(gu) || !aligned16(h) || !aligned16(XA_save) || !aligned16(workspace))
+    return QLORA_ERR_ALIGN;
+  const qlora::LayerDims d = dims_of(M, d_in, d_out, r, s);
+  if (workspace == nullptr || workspace_bytes < qlora::workspace_bytes(d)) return QLORA_ERR_WORKSPACE;
+  int* status = nullptr;
+  st = status_word(&status);
+  if (st != QLORA_OK) return st;
+  cudaError_t e = qlora::run_forward(d, X, packed, absmax, A, B, gu, XA_save, qlora::carve_workspace(d, workspace),
+                                     status, reinterpret_cast<cudaStream_t>(stream), h);
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+qlora_status qlora_linear_bwd_swiglu(const uint16_t* h, const uint16_t* dY, int64_t M, int64_t d_ff,
+                                     int64_t d_out, const uint8_t* packed, const float* absmax,
+                                     const uint16_t* A, const uint16_t* B, int32_t r, float s,
+                                     const float* XA_saved, const uint16_t* gu, uint16_t* dgu, float* dA,
+                                     float* dB, void* workspace, size_t workspace_bytes, qlora_stream_t stream) {
+  if (d_ff < 1 || d_ff > kMaxDim / 2) return QLORA_ERR_SHAPE;
+  if (d_ff % 64 != 0) return QLORA_ERR_UNSUPPORTED;
+  qlora_status st = check_layer(M, d_ff, d_out, r);
+  if (st != QLORA_OK) return st;
+  if (!packed || !absmax || !A || !B || !dA || !dB) return QLORA_ERR_NULL;
+  if (!aligned16(packed) || !aligned16(absmax) || !aligned16(A) || !aligned16(B) || !aligned16(dA) ||
+      !aligned16(dB))
+    return QLORA_ERR_ALIGN;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * static_cast<size_t>(d_ff) * r, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dB, 0, sizeof(float) * static_cast<size_t>(d_out) * r, cs);
+    return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+  }
+  if (!h || !dY || !XA_saved || !gu || !dgu) return QLORA_ERR_NULL;
+  if (!aligned16(h) || !aligned16(dY) || !aligned16(XA_saved) || !aligned16(gu) || !aligned16(dgu) ||
+      !aligned16(workspace))
+    return QLORA_ERR_ALIGN;
+  const qlora::LayerDims d = dims_of(M, d_ff, d_out, r, s);
+  if (workspace == nullptr || workspace_bytes < qlora::workspace_bytes(d)) return QLORA_ERR_WORKSPACE;
+  int* status = nullptr;
+  st = status_word(&status);
+  if (st != QLORA_OK) return st;
+  cudaError_t e = qlora::run_backward(d, h, dY, packed, absmax, A, B, XA_saved, nullptr, dA, dB,
+                                      qlora::carve_workspace(d, workspace), status, cs, gu, dgu);
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+namespace {
+qlora_status check_mlp(int64_t M, int64_t d_model, int64_t d_ff, int32_t r_gu, int32_t r_d) {
+  if (d_ff < 1 || d_ff > kMaxDim / 2) return QLORA_ERR_SHAPE;
+  if (d_ff % 64 != 0) return QLORA_ERR_UNSUPPORTED;
+  const qlora_status a = check_layer(M, d_model, 2 * d_ff, r_gu);
+  return a != QLORA_OK ? a : check_layer(M, d_ff, d_model, r_d);
+}
+}  // namespace
+
+size_t qlora_swiglu_mlp_workspace_bytes(int64_t M, int64_t d_model, int64_t d_ff, int32_t r_gu, int32_t r_d) {
+  if (d_ff < 1 || d_ff > kMaxDim / 2 || d_ff % 64 != 0) return 0;
+  const size_t a = qlora_workspace_bytes(M, d_model, 2 * d_ff, r_gu);
+  const size_t b = qlora_workspace_bytes(M, d_ff, d_model, r_d);
+  if (a == 0 || b == 0) return 0;
+  return a > b ? a : b;
+}
+
+qlora_status qlora_swiglu_mlp_fwd(const uint16_t* X, int64_t M, int64_t d_model, int64_t d_ff,
+                                  const uint8_t* gu_packed, const float* gu_absmax, const uint16_t* A_gu,
+                                  const uint16_t* B_gu, int32_t r_gu, float s_gu, const uint8_t* d_packed,
+                                  const float* d_absmax, const uint16_t* A_d, const uint16_t* B_d, int32_t r_d,
+                                  float s_d, uint16_t* Y, uint16_t* gu, uint16_t* h, float* T_gu, float* T_d,
+                                  void* workspace, size_t workspace_bytes, qlora_stream_t stream) {
+  const qlora_status shape = check_mlp(M, d_model, d_ff, r_gu, r_d);
+  if (shape != QLORA_OK) return shape;
+  if (workspace == nullptr || workspace_bytes < qlora_swiglu_mlp_workspace_bytes(M, d_model, d_ff, r_gu, r_d))
+    return QLORA_ERR_WORKSPACE;
+  qlora_status st = qlora_linear_fwd_swiglu(X, M, d_model, d_ff, gu_packed, gu_absmax, A_gu, B_gu, r_gu, s_gu, gu,
+                                            h, T_gu, workspace, workspace_bytes, stream);
+  if (st != QLORA_OK) return st;
+  return qlora_linear_fwd(h, M, d_ff, d_model, d_packed, d_absmax, A_d, B_d, r_d, s_d, Y, T_d, workspace,
+                          workspace_bytes, stream);
+}
+
+qlora_status qlora_swiglu_mlp_bwd(const uint16_t* X, const uint16_t* dY, int64_t M, int64_t d_model, int64_t d_ff,
+                                  const uint8_t* gu_packed, const float* gu_absmax, const uint16_t* A_gu,
+                                  const uint16_t* B_gu, int32_t r_gu, float s_gu, const uint8_t* d_packed,
+                                  const float* d_absmax, const uint16_t* A_d, const uint16_t* B_d, int32_t r_d,
+                                  float s_d, const uint16_t* gu, const uint16_t* h, const float* T_gu,
+                                  const float* T_d, uint16_t* dgu, uint16_t* dX, float* dA_gu, float* dB_gu,
+                                  float* dA_d, float* dB_d, void* workspace, size_t workspace_bytes,
+                                  qlora_stream_t stream) {
+  const qlora_status shape = check_mlp(M, d_model, d_ff, r_gu, r_d);
+  if (shape != QLORA_OK) return shape;
+  if (workspace == nullptr || workspace_bytes < qlora_swiglu_mlp_workspace_bytes(M, d_model, d_ff, r_gu, r_d))
+    return QLORA_ERR_WORKSPACE;
+  qlora_status st = qlora_linear_bwd_swiglu(h, dY, M, d_ff, d_model, d_packed, d_absmax, A_d, B_d, r_d, s_d, T_d,
+                                            gu, dgu, dA_d, dB_d, workspace, workspace_bytes, stream);
+  if (st != QLORA_OK) return st;
+  return qlora_linear_bwd(X, dgu, M, d_model, 2 * d_ff, gu_packed, gu_absmax, A_gu, B_gu, r_gu, s_gu, T_gu, dX,
+                          dA_gu, dB_gu, workspace, workspace_bytes, stream);
 }
 
 }  // extern "C"

@@ -11,7 +11,9 @@
 // "在ms-swift中的角色").
 //
 // Layout: gu [M, 2*d_ff] is the stacked projection's output, gate columns
-// [0, d_ff) then up columns [d_ff, 2*d_ff); h and dh are [M, d_ff]; the
+// [0, d_ff) then up columns [d_ff, 2*d_ff) -- or, interleaved, 64-column
+// chunks [gate 0..63 | up 0..63 | gate 64..127 | ...], the layout whose gate
+// the main kernel's epilogue computes; h and dh are [M, d_ff]; the
 // backward writes dgu in the layout of gu, which is the dY of the stacked
 // projection's backward.  All bf16; the arithmetic is fp32 with one rounding
 // of each output.  HBM-bound: 6 B per h element forward, 10 B backward.
@@ -34,16 +36,22 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 
 __device__ __forceinline__ float sigmoid(float x) { return 1.f / (1.f + expf(-x)); }
 
+// Column of gate feature f in a row of gu; the up feature is d_ff (or, interleaved, 64) further.
+__device__ __forceinline__ int64_t gate_col(int64_t f, bool interleaved) {
+  return interleaved ? (f >> 6) * 128 + (f & 63) : f;
+}
+
 // One thread: 8 consecutive features of one row (16-byte loads and stores).
 __global__ void __launch_bounds__(256) swiglu_fwd_kernel(const uint16_t* __restrict__ gu, int64_t rows,
-                                                         int64_t d_ff, uint16_t* __restrict__ h) {
+                                                         int64_t d_ff, uint16_t* __restrict__ h, bool interleaved) {
   const int64_t per_row = d_ff / 8, total = rows * per_row;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t m = i / per_row, f = (i % per_row) * 8;
     const uint16_t* row = gu + m * 2 * d_ff;
-    const uint4 g = __ldg(reinterpret_cast<const uint4*>(row + f));
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + d_ff + f));
+    const int64_t gc = gate_col(f, interleaved), uc = gc + (interleaved ? 64 : d_ff);
+    const uint4 g = __ldg(reinterpret_cast<const uint4*>(row + gc));
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + uc));
     const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w};
     uint32_t o[4];
 #pragma unroll
@@ -57,14 +65,15 @@ __global__ void __launch_bounds__(256) swiglu_fwd_kernel(const uint16_t* __restr
 
 __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const uint16_t* __restrict__ gu,
                                                          const uint16_t* __restrict__ dh, int64_t rows,
-                                                         int64_t d_ff, uint16_t* __restrict__ dgu) {
+                                                         int64_t d_ff, uint16_t* __restrict__ dgu, bool interleaved) {
   const int64_t per_row = d_ff / 8, total = rows * per_row;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t m = i / per_row, f = (i % per_row) * 8;
     const uint16_t* row = gu + m * 2 * d_ff;
-    const uint4 g = __ldg(reinterpret_cast<const uint4*>(row + f));
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + d_ff + f));
+    const int64_t gc = gate_col(f, interleaved), uc = gc + (interleaved ? 64 : d_ff);
+    const uint4 g = __ldg(reinterpret_cast<const uint4*>(row + gc));
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(row + uc));
     const uint4 d = __ldg(reinterpret_cast<const uint4*>(dh + m * d_ff + f));
     const uint32_t gw[4] = {g.x, g.y, g.z, g.w}, uw[4] = {u.x, u.y, u.z, u.w}, dw[4] = {d.x, d.y, d.z, d.w};
     uint32_t og[4], ou[4];
@@ -84,8 +93,8 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const uint16_t* __restr
       ou[k] = pack2(du[0], du[1]);
     }
     uint16_t* out = dgu + m * 2 * d_ff;
-    *reinterpret_cast<uint4*>(out + f) = make_uint4(og[0], og[1], og[2], og[3]);
-    *reinterpret_cast<uint4*>(out + d_ff + f) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+    *reinterpret_cast<uint4*>(out + gc) = make_uint4(og[0], og[1], og[2], og[3]);
+    *reinterpret_cast<uint4*>(out + uc) = make_uint4(ou[0], ou[1], ou[2], ou[3]);
   }
 }
 
@@ -99,18 +108,19 @@ int swiglu_grid(int64_t rows, int64_t d_ff) {
 
 }  // namespace
 
-cudaError_t launch_swiglu_fwd(const uint16_t* gu, int64_t rows, int64_t d_ff, uint16_t* h, cudaStream_t stream) {
+cudaError_t launch_swiglu_fwd(const uint16_t* gu, int64_t rows, int64_t d_ff, uint16_t* h, bool interleaved,
+                              cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   LaunchScope scope(kKindSwigluFwd, stream);
-  swiglu_fwd_kernel<<<swiglu_grid(rows, d_ff), 256, 0, stream>>>(gu, rows, d_ff, h);
+  swiglu_fwd_kernel<<<swiglu_grid(rows, d_ff), 256, 0, stream>>>(gu, rows, d_ff, h, interleaved);
   return cudaGetLastError();
 }
 
 cudaError_t launch_swiglu_bwd(const uint16_t* gu, const uint16_t* dh, int64_t rows, int64_t d_ff, uint16_t* dgu,
-                              cudaStream_t stream) {
+                              bool interleaved, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   LaunchScope scope(kKindSwigluBwd, stream);
-  swiglu_bwd_kernel<<<swiglu_grid(rows, d_ff), 256, 0, stream>>>(gu, dh, rows, d_ff, dgu);
+  swiglu_bwd_kernel<<<swiglu_grid(rows, d_ff), 256, 0, stream>>>(gu, dh, rows, d_ff, dgu, interleaved);
   return cudaGetLastError();
 }
 

@@ -33,6 +33,7 @@ _SIGNATURES = {
     "qlora_profile_collect": (ctypes.c_int, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float),
                                              ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "qlora_launch_count": (ctypes.c_int64, []),
+    "qlora_debug_stall_main_launches": (ctypes.c_int, [ctypes.c_int]),
     "qlora_quantize_nf4": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
     "qlora_dequant_nf4": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
     "qlora_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32]),
@@ -46,6 +47,24 @@ _SIGNATURES = {
                                        _c_void_p, _c_void_p]),
     "qlora_swiglu_fwd": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
     "qlora_swiglu_bwd": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
+    "qlora_linear_fwd_swiglu": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p, _c_void_p,
+                                               _c_void_p, _i32, _f32, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                               _sz, _c_void_p]),
+    "qlora_linear_bwd_swiglu": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p,
+                                               _c_void_p, _c_void_p, _i32, _f32, _c_void_p, _c_void_p, _c_void_p,
+                                               _c_void_p, _c_void_p, _c_void_p, _sz, _c_void_p]),
+    "qlora_swiglu_mlp_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32, _i32]),
+    "qlora_swiglu_mlp_fwd": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64,
+                                            _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _f32,
+                                            _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _f32,
+                                            _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                            _c_void_p, _sz, _c_void_p]),
+    "qlora_swiglu_mlp_bwd": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _i64,
+                                            _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _f32,
+                                            _c_void_p, _c_void_p, _c_void_p, _c_void_p, _i32, _f32,
+                                            _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                            _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p,
+                                            _c_void_p, _sz, _c_void_p]),
     "qlora_linear_bwd": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _i64, _c_void_p,
                                         _c_void_p, _c_void_p, _c_void_p, _i32, _f32, _c_void_p,
                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p, _sz,
@@ -135,6 +154,12 @@ def qlora_profile_collect() -> dict:
 
 def qlora_launch_count() -> int:
     return int(load_library().qlora_launch_count())
+
+
+def qlora_debug_stall_main_launches(launches: int) -> None:
+    """Test hook: the next `launches` launches of the fused main kernel load no
+    token operand, so their bounded waits run out and report QLORA_ERR_TIMEOUT."""
+    _check("qlora_debug_stall_main_launches", load_library().qlora_debug_stall_main_launches(int(launches)))
 
 
 def qlora_workspace_bytes(M: int, d_in: int, d_out: int, r: int) -> int:
@@ -290,3 +315,125 @@ def qlora_linear_bwd(X: torch.Tensor, dY: torch.Tensor, packed: torch.Tensor,
         _dev(dB, "dB", torch.float32), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), _stream(X)))
     return dX, dA, dB
+
+
+def qlora_linear_fwd_swiglu(X: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, A: torch.Tensor,
+                            B: torch.Tensor, s: float, *, gu: torch.Tensor | None = None,
+                            h: torch.Tensor | None = None, XA: torch.Tensor | None = None,
+                            workspace: torch.Tensor | None = None):
+    """The interleaved gate/up layer with the SwiGLU gate in its epilogue.
+    Returns (gu [M, 2*d_ff], h [M, d_ff], XA [M, r])."""
+    lib = load_library()
+    M, d_in = X.shape
+    r, two_ff = B.shape
+    d_ff = two_ff // 2
+    if A.shape != (d_in, r):
+        raise ValueError(f"A must be [{d_in}, {r}], got {tuple(A.shape)}")
+    if gu is None:
+        gu = torch.empty(M, two_ff, dtype=torch.bfloat16, device=X.device)
+    if h is None:
+        h = torch.empty(M, d_ff, dtype=torch.bfloat16, device=X.device)
+    if XA is None:
+        XA = torch.empty(M, r, dtype=torch.float32, device=X.device)
+    workspace, _ = _workspace(M, d_in, two_ff, r, X.device, workspace)
+    _check("qlora_linear_fwd_swiglu", lib.qlora_linear_fwd_swiglu(
+        _dev(X, "X", torch.bfloat16), M, d_in, d_ff, _dev(packed, "packed", torch.uint8),
+        _dev(absmax, "absmax", torch.float32), _dev(A, "A", torch.bfloat16), _dev(B, "B", torch.bfloat16), r,
+        float(s), _dev(gu, "gu", torch.bfloat16), _dev(h, "h", torch.bfloat16), _dev(XA, "XA", torch.float32),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(X)))
+    return gu, h, XA
+
+
+def qlora_linear_bwd_swiglu(h: torch.Tensor, dY: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor,
+                            A: torch.Tensor, B: torch.Tensor, s: float, XA: torch.Tensor, gu: torch.Tensor, *,
+                            dgu: torch.Tensor | None = None, dA: torch.Tensor | None = None,
+                            dB: torch.Tensor | None = None, workspace: torch.Tensor | None = None):
+    """The down layer's backward with the gate's backward in its epilogue.
+    Returns (dgu [M, 2*d_ff] interleaved like gu, dA, dB)."""
+    lib = load_library()
+    M, d_ff = h.shape
+    r, d_out = B.shape
+    if dY.shape != (M, d_out) or gu.shape != (M, 2 * d_ff):
+        raise ValueError("dY must be [M, d_out] and gu [M, 2*d_ff]")
+    if dgu is None:
+        dgu = torch.empty(M, 2 * d_ff, dtype=torch.bfloat16, device=h.device)
+    if dA is None:
+        dA = torch.empty(d_ff, r, dtype=torch.float32, device=h.device)
+    if dB is None:
+        dB = torch.empty(r, d_out, dtype=torch.float32, device=h.device)
+    workspace, _ = _workspace(M, d_ff, d_out, r, h.device, workspace)
+    _check("qlora_linear_bwd_swiglu", lib.qlora_linear_bwd_swiglu(
+        _dev(h, "h", torch.bfloat16), _dev(dY, "dY", torch.bfloat16), M, d_ff, d_out,
+        _dev(packed, "packed", torch.uint8), _dev(absmax, "absmax", torch.float32), _dev(A, "A", torch.bfloat16),
+        _dev(B, "B", torch.bfloat16), r, float(s), _dev(XA, "XA", torch.float32), _dev(gu, "gu", torch.bfloat16),
+        _dev(dgu, "dgu", torch.bfloat16), _dev(dA, "dA", torch.float32), _dev(dB, "dB", torch.float32),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(h)))
+    return dgu, dA, dB
+
+
+def qlora_swiglu_mlp_workspace_bytes(M: int, d_model: int, d_ff: int, r_gu: int, r_d: int) -> int:
+    return int(load_library().qlora_swiglu_mlp_workspace_bytes(M, d_model, d_ff, r_gu, r_d))
+
+
+def qlora_swiglu_mlp_fwd(X, gu_layer, d_layer, s_gu: float, s_d: float, *, workspace=None):
+    """The fused SwiGLU block forward; gu_layer / d_layer are (packed, absmax, A, B).
+    Returns (Y, saved) with saved = (gu, h, T_gu, T_d)."""
+    lib = load_library()
+    M, d_model = X.shape
+    pg, ag, Ag, Bg = gu_layer
+    pd, ad, Ad, Bd = d_layer
+    r_gu, r_d = Bg.shape[0], Bd.shape[0]
+    d_ff = Bg.shape[1] // 2
+    dev = X.device
+    Y = torch.empty(M, d_model, dtype=torch.bfloat16, device=dev)
+    gu = torch.empty(M, 2 * d_ff, dtype=torch.bfloat16, device=dev)
+    h = torch.empty(M, d_ff, dtype=torch.bfloat16, device=dev)
+    T_gu = torch.empty(M, r_gu, dtype=torch.float32, device=dev)
+    T_d = torch.empty(M, r_d, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(16, qlora_swiglu_mlp_workspace_bytes(M, d_model, d_ff, r_gu, r_d)),
+                                dtype=torch.uint8, device=dev)
+    _check("qlora_swiglu_mlp_fwd", lib.qlora_swiglu_mlp_fwd(
+        _dev(X, "X", torch.bfloat16), M, d_model, d_ff,
+        _dev(pg, "gu_packed", torch.uint8), _dev(ag, "gu_absmax", torch.float32), _dev(Ag, "A_gu", torch.bfloat16),
+        _dev(Bg, "B_gu", torch.bfloat16), r_gu, float(s_gu),
+        _dev(pd, "d_packed", torch.uint8), _dev(ad, "d_absmax", torch.float32), _dev(Ad, "A_d", torch.bfloat16),
+        _dev(Bd, "B_d", torch.bfloat16), r_d, float(s_d),
+        _dev(Y, "Y", torch.bfloat16), _dev(gu, "gu", torch.bfloat16), _dev(h, "h", torch.bfloat16),
+        _dev(T_gu, "T_gu", torch.float32), _dev(T_d, "T_d", torch.float32),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(X)))
+    return Y, (gu, h, T_gu, T_d)
+
+
+def qlora_swiglu_mlp_bwd(X, dY, saved, gu_layer, d_layer, s_gu: float, s_d: float, *, need_dX: bool = True,
+                         workspace=None):
+    """The fused SwiGLU block backward.  Returns dX, (dA_gu, dB_gu), (dA_d, dB_d)."""
+    lib = load_library()
+    M, d_model = X.shape
+    gu, h, T_gu, T_d = saved
+    pg, ag, Ag, Bg = gu_layer
+    pd, ad, Ad, Bd = d_layer
+    r_gu, r_d = Bg.shape[0], Bd.shape[0]
+    d_ff = Bg.shape[1] // 2
+    dev = X.device
+    dgu = torch.empty(M, 2 * d_ff, dtype=torch.bfloat16, device=dev)
+    dX = torch.empty(M, d_model, dtype=torch.bfloat16, device=dev) if need_dX else None
+    dA_gu = torch.empty(d_model, r_gu, dtype=torch.float32, device=dev)
+    dB_gu = torch.empty(r_gu, 2 * d_ff, dtype=torch.float32, device=dev)
+    dA_d = torch.empty(d_ff, r_d, dtype=torch.float32, device=dev)
+    dB_d = torch.empty(r_d, d_model, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(16, qlora_swiglu_mlp_workspace_bytes(M, d_model, d_ff, r_gu, r_d)),
+                                dtype=torch.uint8, device=dev)
+    _check("qlora_swiglu_mlp_bwd", lib.qlora_swiglu_mlp_bwd(
+        _dev(X, "X", torch.bfloat16), _dev(dY, "dY", torch.bfloat16), M, d_model, d_ff,
+        _dev(pg, "gu_packed", torch.uint8), _dev(ag, "gu_absmax", torch.float32), _dev(Ag, "A_gu", torch.bfloat16),
+        _dev(Bg, "B_gu", torch.bfloat16), r_gu, float(s_gu),
+        _dev(pd, "d_packed", torch.uint8), _dev(ad, "d_absmax", torch.float32), _dev(Ad, "A_d", torch.bfloat16),
+        _dev(Bd, "B_d", torch.bfloat16), r_d, float(s_d),
+        _dev(gu, "gu", torch.bfloat16), _dev(h, "h", torch.bfloat16), _dev(T_gu, "T_gu", torch.float32),
+        _dev(T_d, "T_d", torch.float32), _dev(dgu, "dgu", torch.bfloat16),
+        _dev(dX, "dX", torch.bfloat16) if dX is not None else None, _dev(dA_gu, "dA_gu", torch.float32),
+        _dev(dB_gu, "dB_gu", torch.float32), _dev(dA_d, "dA_d", torch.float32), _dev(dB_d, "dB_d", torch.float32),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(X)))
+    return dX, (dA_gu, dB_gu), (dA_d, dB_d)

@@ -130,3 +130,9 @@ def test_swiglu_argument_validation(lib):
     assert fwd(gu=None) == 1 and bwd(dh=None) == 1 and bwd(dgu=None) == 1
     assert fwd(h=MISALIGNED) == 3 and bwd(gu=MISALIGNED) == 3
     assert fwd(M=0, gu=None, h=None) == 0 and bwd(M=0, gu=None, dh=None, dgu=None) == 0
+
+
+def test_stall_hook_is_off_by_default_and_rejects_negative(lib):
+    from rank_adapter_linear_nf4_b300 import qlora
+    assert lib.qlora_debug_stall_main_launches(-1) == 2     # QLORA_ERR_SHAPE, nothing armed
+    assert lib.qlora_debug_stall_main_launches(0) == 0

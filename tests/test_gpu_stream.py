@@ -1,11 +1,12 @@
 """The forward for 1..16 tokens (the NF4 weight-stream kernel) against the oracle.
 
 Same bar as the other layer tests: per output tensor, max|gpu - oracle| <=
-1e-2 * max|oracle|, every element compared.  The kernel splits the items
-(32 weight rows x one 64-element block) evenly over its warps; the cases walk
-ranges inside one row pair, ranges crossing several row pairs (short d_in),
-row pairs shared by many warps (long d_in), ragged last pairs (d_out % 32 !=
-0), ranks 1..128 and token counts on both sides of 8.
+1e-2 * max|oracle|, every element compared.  The kernel splits its items (16
+weight rows x 256 input features) evenly over CTAs and warps, in units of 16
+rows x 1024 features; the cases walk units split between two warps or CTAs,
+row groups summed over many slices (long d_in), a last slice shorter than
+1024, ragged last row groups (d_out % 16 != 0), ranks 1..128 and token counts
+on both sides of 8.  d_in % 256 != 0 goes to the main kernel.
 Low-rank-dominant cases (zero base weight, B ~ N(0, 1)) check that term on its
 own, since with the standard scales it is only a few percent of Y.
 """
@@ -26,19 +27,19 @@ def _inputs(M, K, N, r, seed=0, b_std=0.01):
 
 CASES = [
     # (M, d_in, d_out, r, s); an item is 32 weight rows x one 64-element block
-    (1, 256, 256, 16, 1.0),         # 8 row pairs of 4 items: one warp's range spans row pairs
+    (1, 256, 256, 16, 1.0),         # 16 units of one item
     (3, 256, 64, 8, 2.0),           # a single CTA
-    (8, 4096, 64, 16, 1.0),         # two row pairs of 64 items, each summed over several warps
-    (9, 512, 136, 24, 0.5),         # two token groups with 9 tokens; last row pair has 8 rows
-    (16, 512, 14336, 128, 0.25),    # 448 row pairs; rank 128
-    (5, 14336, 256, 64, 0.25),      # long contraction: 8 row pairs of 224 items, ~56 warps each
+    (8, 4096, 64, 16, 1.0),         # four slices per row group
+    (9, 512, 136, 24, 0.5),         # two token groups with 9 tokens; last group 8 rows; units split
+    (16, 512, 14336, 128, 0.25),    # 896 row groups; rank 128
+    (5, 14336, 256, 64, 0.25),      # long contraction: 14 slices per row group
     (16, 4096, 4096, 16, 1.0),      # the q_proj layer at 16 tokens
-    (12, 512, 200, 65, 1.25),       # rank padded to 128, A padded (r % 8 != 0), last pair 8 rows
-    (2, 256, 8, 1, 3.0),            # one 8-row pair (24 rows past d_out), rank 1
-    (4, 1024, 64 * 148 + 8, 16, 0.5),   # 297 row pairs, the last one 8 rows
-    (7, 64, 14336, 32, 0.5),        # one block per row: each warp's range crosses 4 row pairs
-    (16, 320, 96, 48, 1.0),         # d_in % 256 != 0
-    (1, 192, 40, 4, 2.0),           # d_in = 3 blocks, last pair 8 rows
+    (12, 512, 200, 65, 1.25),       # rank padded to 128, A padded (r % 8 != 0), last group 8 rows
+    (2, 256, 8, 1, 3.0),            # one 8-row group (8 rows past d_out), rank 1
+    (4, 1024, 64 * 148 + 8, 16, 0.5),   # 593 row groups, the last one 8 rows
+    (7, 1280, 14336, 32, 0.5),      # a last slice of 256 features
+    (16, 320, 96, 48, 1.0),         # d_in % 256 != 0: the main kernel
+    (1, 192, 40, 4, 2.0),           # d_in % 256 != 0: the main kernel
 ]
 
 
@@ -65,9 +66,9 @@ def test_stream_with_backward():
 def test_stream_kernel_is_the_one_launched():
     from rank_adapter_linear_nf4_b300 import qlora
     dev = torch.device("cuda", 0)
-    # 1..16 tokens take the stream kernel, more tokens the main kernel
+    # 1..16 tokens with d_in % 256 == 0 take the stream kernel, the rest the main kernel
     for M, K, want, other in ((16, 256, "lora_stream_fwd", "lora_main_fwd"), (17, 256, "lora_main_fwd", "lora_stream_fwd"),
-                              (4, 320, "lora_stream_fwd", "lora_main_fwd")):
+                              (4, 320, "lora_main_fwd", "lora_stream_fwd")):
         inp = _inputs(M, K, 256, 16, seed=M)
         X, W, A, B = (inp[k].to(dev) for k in ("X", "W", "A", "B"))
         packed, absmax = qlora.qlora_quantize_nf4(W)
@@ -82,8 +83,8 @@ def test_stream_kernel_is_the_one_launched():
 
 
 def test_stream_repeat_is_bitwise_identical():
-    """Row pairs shared by warps are summed by whichever warp arrives last, in
-    warp order: repeated calls give the same bits."""
+    """Row groups are summed by whichever warp completes them last, in slice and
+    part order: repeated calls give the same bits."""
     inp = _inputs(16, 4096, 14336, 64, seed=2)
     a = run_gpu(inp, 0.25, bwd=False)
     for _ in range(3):

@@ -5,7 +5,8 @@ one bf16 ulp (the kernel computes in fp32 and rounds once), besides the layer
 bar max|gpu - oracle| <= 1e-2 max|oracle|.  The block (stacked gate/up layer,
 gate, down layer, and the backward through all three) is checked at the layer
 bar against the oracle's composition, whose intermediates are stored in bf16
-as the block stores them.
+as the block stores them -- both the unfused block (a separate gate pass) and
+the fused one (the gate in the layers' epilogues, gate/up rows interleaved).
 """
 import numpy as np
 import pytest
@@ -66,8 +67,8 @@ def test_swiglu_mlp_block(M, d_model, d_ff, r, s):
     gate_up = mlp.Layer(pk_gu, am_gu, A_gu.to(dev), B_gu.to(dev))
     down = mlp.Layer(pk_d, am_d, Ad.to(dev), Bd.to(dev))
     Xd = X.to(dev)
-    Y, saved = mlp.swiglu_mlp_fwd(Xd, gate_up, down, s)
-    dX, (dA_gu, dB_gu), (dA_d, dB_d) = mlp.swiglu_mlp_bwd(Xd, dY.to(dev), saved, gate_up, down, s)
+    Y, saved = mlp.swiglu_mlp_fwd_unfused(Xd, gate_up, down, s)
+    dX, (dA_gu, dB_gu), (dA_d, dB_d) = mlp.swiglu_mlp_bwd_unfused(Xd, dY.to(dev), saved, gate_up, down, s)
     torch.cuda.synchronize()
     assert qlora.qlora_device_status(clear=True) == 0
 
@@ -88,3 +89,86 @@ def test_swiglu_mlp_block(M, d_model, d_ff, r, s):
     for i in range(2):
         assert_close(f"dA_gu{i}", dA_gu_i[i].cpu().numpy(), dA_ref_i[i].numpy())
         assert_close(f"dB_gu{i}", dB_gu_i[i].cpu().numpy(), dB_ref_i[i].numpy())
+
+
+def _block_case(M, d_model, d_ff, r, s, seed=21):
+    X, _ = synthetic.activations(M, d_model, d_model, seed)
+    Wg, Ag, Bg = synthetic.weights(d_model, d_ff, r, seed + 1)
+    Wu, Au, Bu = synthetic.weights(d_model, d_ff, r, seed + 2)
+    Wd, Ad, Bd = synthetic.weights(d_ff, d_model, r, seed + 3)
+    dY = torch.randn(M, d_model, generator=torch.Generator().manual_seed(seed + 4)).to(torch.bfloat16)
+    return X, dY, (Wg, Ag, Bg), (Wu, Au, Bu), (Wd, Ad, Bd)
+
+
+def _oracle_block(X, dY, g, u, d, s):
+    (Wg, Ag, Bg), (Wu, Au, Bu), (Wd, Ad, Bd) = g, u, d
+    A_gu, B_gu = multi.stack_adapters([Ag, Au], [Bg, Bu])
+    W_gu = multi.stack_weights([Wg, Wu])
+    d_ff, d_model = Wg.shape
+    q, a = O.quantize_nf4(np32(W_gu))
+    Wd_gu = O.dequantize_nf4(q, a, 2 * d_ff, d_model)
+    q, a = O.quantize_nf4(np32(Wd))
+    Wd_d = O.dequantize_nf4(q, a, d_model, d_ff)
+    args = (Wd_gu, np32(A_gu), np32(B_gu), Wd_d, np32(Ad), np32(Bd), s)
+    Y_ref, saved_ref = O.swiglu_mlp_forward(np32(X), *args)
+    grads = O.swiglu_mlp_backward(np32(X), np32(dY), saved_ref, *args)
+    return Y_ref, saved_ref, grads
+
+
+def _fused_block(X, dY, g, u, d, s):
+    from rank_adapter_linear_nf4_b300 import qlora
+    (Wg, Ag, Bg), (Wu, Au, Bu), (Wd, Ad, Bd) = g, u, d
+    dev = torch.device("cuda", 0)
+    W_int = mlp.interleave_weights(Wg, Wu)
+    A_cat, B_int = mlp.interleave_adapters(Ag, Bg, Au, Bu)
+    pk_gu, am_gu = qlora.qlora_quantize_nf4(W_int.to(dev))
+    pk_d, am_d = qlora.qlora_quantize_nf4(Wd.to(dev))
+    gate_up = mlp.Layer(pk_gu, am_gu, A_cat.to(dev), B_int.to(dev))
+    down = mlp.Layer(pk_d, am_d, Ad.to(dev), Bd.to(dev))
+    Xd = X.to(dev)
+    Y, saved = mlp.swiglu_mlp_fwd(Xd, gate_up, down, s)
+    dX, (dA_gu, dB_gu), (dA_d, dB_d) = mlp.swiglu_mlp_bwd(Xd, dY.to(dev), saved, gate_up, down, s)
+    torch.cuda.synchronize()
+    assert qlora.qlora_device_status(clear=True) == 0
+    return Y, saved, dX, (dA_gu, dB_gu), (dA_d, dB_d)
+
+
+@pytest.mark.parametrize("M,d_model,d_ff,r,s", [(192, 512, 1408, 32, 0.5),      # BN 256, whole tiles
+                                                (8, 1024, 2816, 64, 0.25),      # forward through the weight stream
+                                                (40, 4096, 256, 16, 1.0),       # dX tiles split across CTAs
+                                                (2048, 512, 1024, 16, 2.0)],    # BN 512
+                         ids=lambda v: str(v))
+def test_swiglu_mlp_block_fused(M, d_model, d_ff, r, s):
+    """The block with the gate in the layers' epilogues against the oracle's composition."""
+    X, dY, g, u, d = _block_case(M, d_model, d_ff, r, s)
+    Y, (gu, h, T_gu, T_d), dX, (dA_gu, dB_gu), (dA_d, dB_d) = _fused_block(X, dY, g, u, d, s)
+    Y_ref, (gu_ref, T_gu_ref, h_ref, T_d_ref), grads = _oracle_block(X, dY, g, u, d, s)
+    dX_ref, (dA_gu_ref, dB_gu_ref), (dA_d_ref, dB_d_ref) = grads
+    assert_close("gu", np32(mlp.deinterleave(gu)), gu_ref)
+    assert_close("h", np32(h), h_ref)
+    assert_close("Y", np32(Y), Y_ref)
+    assert_close("dX", np32(dX), dX_ref)
+    assert_close("dA_d", dA_d.cpu().numpy(), dA_d_ref)
+    assert_close("dB_d", dB_d.cpu().numpy(), dB_d_ref)
+    r_g = g[1].shape[1]
+    (dAg, dBg), (dAu, dBu) = mlp.split_adapter_grads(dA_gu.cpu(), dB_gu.cpu(), r_g)
+    d_ff_ = d[0].shape[1]
+    assert_close("dA_gate", dAg.numpy(), dA_gu_ref[:, :r_g])
+    assert_close("dA_up", dAu.numpy(), dA_gu_ref[:, r_g:])
+    assert_close("dB_gate", dBg.numpy(), dB_gu_ref[:r_g, :d_ff_])
+    assert_close("dB_up", dBu.numpy(), dB_gu_ref[r_g:, d_ff_:])
+
+
+def test_fused_block_launches_no_gate_pass():
+    """With more than 16 tokens the fused block launches the layer kernels only."""
+    from rank_adapter_linear_nf4_b300 import qlora
+    X, dY, g, u, d = _block_case(64, 512, 1024, 16, 1.0, seed=5)
+    _fused_block(X, dY, g, u, d, 1.0)   # warm (tensor maps, first launches)
+    qlora.qlora_profile_enable(True)
+    qlora.qlora_profile_collect()
+    _fused_block(X, dY, g, u, d, 1.0)
+    prof = qlora.qlora_profile_collect()
+    qlora.qlora_profile_enable(False)
+    assert "swiglu_fwd" not in prof and "swiglu_bwd" not in prof, prof
+    assert prof["lora_main_fwd"][1] == 2 and prof["lora_main_dX"][1] == 2, prof
+
