@@ -63,7 +63,9 @@ typedef enum qlora_status {
   QLORA_ERR_UNSUPPORTED = 4,  /* d_in % 64 != 0, d_out % 8 != 0, r outside [1, 128] */
   QLORA_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed; see qlora_last_cuda_error() */
   QLORA_ERR_TIMEOUT = 6,      /* a bounded device-side wait ran out (see qlora_device_status) */
-  QLORA_ERR_WORKSPACE = 7     /* workspace NULL or smaller than qlora_workspace_bytes() */
+  QLORA_ERR_WORKSPACE = 7,    /* workspace NULL or smaller than qlora_workspace_bytes() */
+  QLORA_ERR_INTERNAL = 8      /* a kernel found its shared-memory layout does not fit its launch
+                                 (recorded in the device status word; nothing was computed) */
 } qlora_status;
 
 struct CUstream_st;

@@ -101,6 +101,8 @@ struct SkinnyParams {
   uint16_t* s_t;       // kRowsG: bf16(s*T) [rows, RP] written from xa
   int* zero;           // rows modes: split-tile counters of the main kernel that follows
   int n_zero;
+  int wait_first;      // launched with programmatic serialisation as a call's first kernel:
+                       // wait for the previous kernel before touching global memory
   int* status;
 };
 
@@ -160,15 +162,12 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const int nct = ct_end - ct_begin;
   Abort ab{&s_abort, p.status};
 
-  if (MODE != kRed && blockIdx.x == 0 && blockIdx.y == 0) {
-    // the main kernel after this one counts finished pieces of its split tiles
-    // from zero; it reads the counters only after waiting for this kernel
-    for (int i = static_cast<int>(threadIdx.x); i < p.n_zero; i += kSkThreads) p.zero[i] = 0;
-  }
   if (threadIdx.x == 0) {
     // a dependent kernel may be scheduled now: it waits (griddepcontrol.wait)
-    // before it reads anything this kernel writes
-    griddep_launch_dependents();
+    // before it reads anything this kernel writes.  It does read the call's
+    // inputs before that wait, so a kernel that itself started early lets it
+    // go only after its own wait (below).
+    if (!p.wait_first) griddep_launch_dependents();
     s_abort = 0;
     for (int i = 0; i < S::kStages; ++i) {
       mbar_init(bar0 + 8u * i, 1);                    // full
@@ -186,6 +185,17 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_d = s_tmem;
+  // as a call's first kernel this one may start while the previous kernel on the
+  // stream runs: the set-up above overlaps it, the reads and writes below wait
+  if (p.wait_first) {
+    griddep_wait();
+    if (threadIdx.x == 0) griddep_launch_dependents();
+  }
+  if (MODE != kRed && blockIdx.x == 0 && blockIdx.y == 0) {
+    // the main kernel after this one counts finished pieces of its split tiles
+    // from zero; it reads the counters only after waiting for this kernel
+    for (int i = static_cast<int>(threadIdx.x); i < p.n_zero; i += kSkThreads) p.zero[i] = 0;
+  }
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1136,8 +1146,9 @@ cudaError_t launch_skinny_split(const CUtensorMap (&maps)[4], const SkinnyParams
   }
 }
 
-// `pdl`: launched with programmatic serialisation -- only for a kernel whose
-// inputs were complete before the previous kernel on the stream started.
+// `pdl`: launched with programmatic serialisation -- for a kernel whose inputs
+// were complete before the previous kernel on the stream started, or one that
+// waits for that kernel before it touches global memory (sp.wait_first).
 template <int MODE>
 cudaError_t launch_skinny(int rp, const CUtensorMap (&maps)[4], const SkinnyParams& sp, int tiles,
                           int split, cudaStream_t stream, bool pdl = false) {
@@ -1390,7 +1401,8 @@ cudaError_t run_forward(const LayerDims& d, const uint16_t* X, const uint8_t* pa
     sp.n_zero = ws.counters != nullptr ? ws.counter_cap : 0;
     sp.status = status;
     const int tiles = sp.job[0].tiles;
-    e = launch_skinny<kRowsT>(d.rp, maps, sp, tiles, pick_split(tiles, sp.num_ct), stream);
+    sp.wait_first = 1;
+    e = launch_skinny<kRowsT>(d.rp, maps, sp, tiles, pick_split(tiles, sp.num_ct), stream, true);
     if (e != cudaSuccess) return e;
   }
   GateIo gate;
@@ -1427,7 +1439,8 @@ cudaError_t run_backward(const LayerDims& d, const uint16_t* X, const uint16_t* 
     sp.n_zero = ws.counters != nullptr ? ws.counter_cap : 0;
     sp.status = status;
     const int tiles = sp.job[0].tiles;
-    e = launch_skinny<kRowsG>(d.rp, maps, sp, tiles, pick_split(tiles, sp.num_ct), stream);
+    sp.wait_first = 1;
+    e = launch_skinny<kRowsG>(d.rp, maps, sp, tiles, pick_split(tiles, sp.num_ct), stream, true);
     if (e != cudaSuccess) return e;
   }
   // dX first; the dA/dB kernel then runs in the SMs dX's last tiles leave idle.  It may start

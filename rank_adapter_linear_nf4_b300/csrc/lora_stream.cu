@@ -60,15 +60,15 @@
 namespace qlora {
 namespace {
 
-constexpr int kWarps = 16;                    // warps per CTA (one CTA per SM)
-constexpr int kThreads = kWarps * 32;
 constexpr int kGroupRows = 16;                // weight rows per unit (one MMA row group)
 constexpr int kItemBlocks = 4;                // NF4 blocks per item (one 128-byte code row)
 constexpr int kSliceBlocks = 16;              // NF4 blocks per unit (1024 input features)
-constexpr int kDepth = 4;                     // items in flight per warp
+constexpr int kDepth = 3;                     // items in flight per warp
 constexpr int kCodeSlot = kGroupRows * 128;   // bytes of codes per item
 constexpr int kAbsSlot = kGroupRows * 16;     // bytes of absmax per item
-constexpr int kLutWords = 256 * 32;           // 256 code bytes x 32 lane copies
+constexpr uint32_t kLutAlign = 65536;         // the decode table starts on a 64 KB boundary
+constexpr int kLutEntry = 256;                // bytes per table entry (32 lane copies in the first 128)
+constexpr int kLutBytes = 256 * kLutEntry;
 constexpr int kXPitch = kSliceBlocks * 64 * 2 + 16;   // bytes per token row of a staged X slice
 
 // bf16 bit patterns (round to nearest even) of the NF4 levels, in code order:
@@ -78,20 +78,46 @@ constexpr uint16_t kLevelBf16[16] = {0xBF80, 0xBF32, 0xBF06, 0xBECA, 0xBE92, 0xB
 __constant__ uint16_t c_level_bf16[16] = {0xBF80, 0xBF32, 0xBF06, 0xBECA, 0xBE92, 0xBE3D, 0xBDBA, 0x0000,
                                           0x3DA3, 0x3E25, 0x3E7C, 0x3EAD, 0x3EE2, 0x3F10, 0x3F39, 0x3F80};
 
-// Shared memory (from a 1024-aligned base, for the swizzled code slots).
+// Warps per CTA (one CTA per SM).  (20 warps at one 8-token MMA column block,
+// which the registers allow, measured slower than 16.)
 template <int MT>
-struct StreamSmem {
-  static constexpr int kXRows = 8 * MT;
-  static constexpr int kCodeOff = 0;
-  static constexpr int kAbsOff = kCodeOff + kWarps * kDepth * kCodeSlot;
-  static constexpr int kLutOff = kAbsOff + kWarps * kDepth * kAbsSlot;
-  static constexpr int kXOff = kLutOff + kLutWords * 4;
-  static constexpr int kBarOff = kXOff + kXRows * kXPitch;
-  static constexpr int kBytes = kBarOff + 8 * (kWarps * kDepth + 1) + 1024;
-  static_assert(kCodeSlot % 1024 == 0, "code slots keep the 128-byte swizzle alignment");
-  static_assert(kXOff % 16 == 0 && kXPitch % 16 == 0, "bulk copies need 16-byte alignment");
-  static_assert(kBytes <= 227 * 1024, "fits the shared memory of one CTA");
+struct StreamCfg {
+  static constexpr int kWarps = 16;
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kSlots = kWarps * kDepth;
 };
+
+// Shared memory.  The decode table sits on a 64 KB boundary so that one prmt
+// forms a lookup address (table | byte << 8 | lane << 2); the code slots
+// (1024-aligned, for the 128-byte swizzle) fill the space below it and, with
+// the absmax slots, the staged X slice and the barriers, the space above.
+template <int MT>
+struct StreamLayout {
+  static constexpr int kSlots = StreamCfg<MT>::kSlots;
+  static constexpr int kXRows = 8 * MT;   // token rows of the X slice, then one row of zeros
+  uint32_t code_lo, n_lo;   // slots 0 .. n_lo-1 below the table
+  uint32_t lut;
+  uint32_t code_hi;         // slots n_lo .. kSlots-1 above it
+  uint32_t abs, x, bar, end;
+  __device__ __forceinline__ explicit StreamLayout(uint32_t window) {
+    code_lo = (window + 1023u) & ~1023u;
+    lut = (code_lo + kLutAlign - 1u) & ~(kLutAlign - 1u);
+    uint32_t n = (lut - code_lo) / kCodeSlot;
+    n -= n % kDepth;                                   // a warp's ring never straddles the table
+    n_lo = n < static_cast<uint32_t>(kSlots) ? n : static_cast<uint32_t>(kSlots);
+    code_hi = lut + kLutBytes;
+    abs = code_hi + (kSlots - n_lo) * kCodeSlot;
+    x = abs + kSlots * kAbsSlot;
+    bar = x + (kXRows + 1) * kXPitch;
+    end = bar + 8u * (kSlots + 1);
+  }
+  __device__ __forceinline__ uint32_t ring(int warp) const {
+    const uint32_t j = static_cast<uint32_t>(warp * kDepth);
+    return j < n_lo ? code_lo + j * kCodeSlot : code_hi + (j - n_lo) * kCodeSlot;
+  }
+};
+static_assert(kCodeSlot % 1024 == 0 && kLutBytes % 1024 == 0, "code slots keep the 128-byte swizzle alignment");
+static_assert(kXPitch % 16 == 0 && kAbsSlot % 16 == 0, "bulk copies need 16-byte alignment");
 
 struct StreamParams {
   const uint16_t* X;        // [M, K] bf16
@@ -130,37 +156,17 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// The pair-table word of code byte `sel & 3` of w, from this lane's copy
-// (entry v of lane l at byte offset 128 v + 4 l; lut_lane = table + 4 l).
+// The pair-table word of code byte i of w from this lane's copy: the address
+// is the table base with the byte in bits 8-15 and 4 * lane in bits 0-7
+// (lut_lane), assembled by one prmt with selector 0x7604 | i << 4.
 __device__ __forceinline__ uint32_t lut_pair(uint32_t lut_lane, uint32_t w, uint32_t sel) {
-  return lds32(prmt(w, 0u, sel) * 128u + lut_lane);
+  return lds32(prmt(w, lut_lane, sel));
 }
 
 // Blocks of slice s.
 __device__ __forceinline__ int slice_blocks(const StreamParams& p, int s) {
   return min(kSliceBlocks, p.kb - s * kSliceBlocks);
 }
-
-// Items of unit u.
-__device__ __forceinline__ int unit_items(const StreamParams& p, int u) {
-  return slice_blocks(p, u / p.groups) / kItemBlocks;
-}
-
-// A position in a slice's item list: unit u, item `it` of the unit.
-struct ItemCursor {
-  int u, it;
-  __device__ __forceinline__ void set(const StreamParams& p, int s, int i) {
-    const int ipu = slice_blocks(p, s) / kItemBlocks;
-    u = s * p.groups + i / ipu;
-    it = i % ipu;
-  }
-  __device__ __forceinline__ void next(const StreamParams& p) {
-    if (++it == unit_items(p, u)) {
-      it = 0;
-      ++u;
-    }
-  }
-};
 
 // The static split of slice s's items: CTA `sub` of the slice takes items
 // [n*sub/cps, n*(sub+1)/cps), and its `active` warps equal parts of those.
@@ -169,28 +175,33 @@ struct SliceSplit {
   __device__ __forceinline__ int cta_begin(const StreamParams& p, int sub) const {
     return static_cast<int>(static_cast<int64_t>(n) * sub / p.cps);
   }
-  __device__ __forceinline__ static int active_warps(int n_cta) { return min(kWarps, max(1, n_cta / kItemBlocks)); }
+  template <int W>
+  __device__ __forceinline__ static int active_warps(int n_cta) { return min(W, max(1, n_cta / kItemBlocks)); }
 };
 
-// One item's MMAs: acc += absmax * (codes of 16 rows x 4 blocks) . X.
+// One item's MMAs: acc += absmax * (codes of 16 rows x 4 blocks) . X.  Lanes
+// of token rows at or past M read the row of zeros (one address for all of
+// them; their MMA columns are never stored).
 template <int MT>
-__device__ __forceinline__ void compute_item(uint32_t code_slot, uint32_t abs_slot, uint32_t x_row0, int blk0,
-                                             uint32_t lut_lane, int g4, int t, float (&acc)[MT][4]) {
+__device__ __forceinline__ void compute_item(uint32_t code_slot, uint32_t abs_slot, const uint32_t (&x_rows)[MT],
+                                             int blk0, uint32_t lut_lane, int g4, int t, float (&acc)[MT][4]) {
+  const uint32_t ra = static_cast<uint32_t>(g4), rb = static_cast<uint32_t>(g4 + 8);
+  const uint4 am_a4 = ld_shared_v4(abs_slot + ra * 16u);   // the item's four block scales, rows g and g+8
+  const uint4 am_b4 = ld_shared_v4(abs_slot + rb * 16u);
 #pragma unroll
   for (int blk = 0; blk < kItemBlocks; ++blk) {
     // rows g and g+8, bytes 8t .. 8t+7 of block blk: 16-byte chunk 2*blk + t/2,
-    // swizzled by the row (128-byte swizzle), half t%2 of it
+    // swizzled by the row (128-byte swizzle; rows g and g+8 swizzle alike), half t%2 of it
     const uint32_t chunk = static_cast<uint32_t>(2 * blk + (t >> 1));
-    const uint32_t ra = static_cast<uint32_t>(g4), rb = static_cast<uint32_t>(g4 + 8);
-    const uint2 ca = lds64(code_slot + ra * 128u + ((chunk ^ (ra & 7u)) << 4) + 8u * (t & 1));
-    const uint2 cb = lds64(code_slot + rb * 128u + ((chunk ^ (rb & 7u)) << 4) + 8u * (t & 1));
-    const float am_a = ld_shared_f32(abs_slot + ra * 16u + blk * 4u);
-    const float am_b = ld_shared_f32(abs_slot + rb * 16u + blk * 4u);
+    const uint32_t ca_addr = code_slot + ra * 128u + ((chunk ^ (ra & 7u)) << 4) + 8u * (t & 1);
+    const uint2 ca = lds64(ca_addr);
+    const uint2 cb = lds64(ca_addr + 1024u);
+    const float am_a = __uint_as_float(blk == 0 ? am_a4.x : blk == 1 ? am_a4.y : blk == 2 ? am_a4.z : am_a4.w);
+    const float am_b = __uint_as_float(blk == 0 ? am_b4.x : blk == 1 ? am_b4.y : blk == 2 ? am_b4.z : am_b4.w);
     uint4 x[MT][2];
 #pragma unroll
     for (int j = 0; j < MT; ++j) {
-      const uint32_t src = x_row0 + static_cast<uint32_t>(j * 8 * kXPitch) +
-                           static_cast<uint32_t>(((blk0 + blk) * 64 + 16 * t) * 2);
+      const uint32_t src = x_rows[j] + static_cast<uint32_t>(((blk0 + blk) * 64 + 16 * t) * 2);
       x[j][0] = ld_shared_v4(src);
       x[j][1] = ld_shared_v4(src + 16);
     }
@@ -201,8 +212,8 @@ __device__ __forceinline__ void compute_item(uint32_t code_slot, uint32_t abs_sl
     for (int s = 0; s < 4; ++s) {
       // k-step s: code bytes 2s (fragment columns 2t, 2t+1) and 2s+1 (2t+8, 2t+9)
       const uint32_t wa = s < 2 ? ca.x : ca.y, wb = s < 2 ? cb.x : cb.y;
-      const uint32_t sel0 = 0x4440u | static_cast<uint32_t>((2 * s) & 3);
-      const uint32_t sel1 = 0x4440u | static_cast<uint32_t>((2 * s + 1) & 3);
+      const uint32_t sel0 = 0x7604u | (static_cast<uint32_t>((2 * s) & 3) << 4);
+      const uint32_t sel1 = 0x7604u | (static_cast<uint32_t>((2 * s + 1) & 3) << 4);
       const uint32_t a[4] = {lut_pair(lut_lane, wa, sel0), lut_pair(lut_lane, wb, sel0),
                              lut_pair(lut_lane, wa, sel1), lut_pair(lut_lane, wb, sel1)};
 #pragma unroll
@@ -294,48 +305,62 @@ __device__ __forceinline__ void finish_group(const StreamParams& p, int group, i
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(StreamCfg<MT>::kThreads, 1)
     lora_stream_kernel(const __grid_constant__ CUtensorMap map_codes,   // [N, K/2] bytes, box {128, 16}, 128-B swizzle
                        const __grid_constant__ CUtensorMap map_abs,     // [N, K/64] fp32, box {4, 16}
                        const StreamParams p) {
-  using S = StreamSmem<MT>;
+  using L = StreamLayout<MT>;
+  constexpr int kWarps = StreamCfg<MT>::kWarps;
+  constexpr int kThreads = StreamCfg<MT>::kThreads;
+  constexpr int kSlots = StreamCfg<MT>::kSlots;
   extern __shared__ uint8_t smem_raw[];
   __shared__ int s_abort;
-  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
-  uint8_t* const gbase = smem_raw + (base - smem_u32(smem_raw));
+  const uint32_t window = smem_u32(smem_raw);
+  const L lay(window);
+  uint32_t dyn_bytes;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn_bytes));
+  if (lay.end > window + dyn_bytes) {
+    // the layout needs more shared memory than the launch gave: compute nothing
+    if (threadIdx.x == 0) atomicExch(p.status, kStatusInternal);
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g4 = lane >> 2, t = lane & 3;
 
-  // this CTA's slice and items, and this warp's part of them
+  // this CTA's slice and items, and this warp's part of them; every unit of
+  // the slice has the same number of items (ipu), so the cursors below step
+  // through (group, item) pairs without divisions
   const int slice = blockIdx.x / p.cps, sub = blockIdx.x % p.cps;
-  const SliceSplit split{p.groups * (slice_blocks(p, slice) / kItemBlocks)};
+  const int ipu = slice_blocks(p, slice) / kItemBlocks;
+  const SliceSplit split{p.groups * ipu};
   const int i_begin = split.cta_begin(p, sub), i_end = split.cta_begin(p, sub + 1);
   const int n_cta = i_end - i_begin;
-  const int active = SliceSplit::active_warps(n_cta);   // at least four items per warp
+  const int active = SliceSplit::active_warps<kWarps>(n_cta);   // at least four items per warp
   const int w_lo = warp < active ? i_begin + n_cta * warp / active : i_end;
   const int w_hi = warp < active ? i_begin + n_cta * (warp + 1) / active : i_end;
   const int n_items = w_hi - w_lo;
-  const uint32_t x_bar = base + S::kBarOff + 8u * (kWarps * kDepth);
-  auto full = [&](int slot) { return base + S::kBarOff + 8u * static_cast<uint32_t>(warp * kDepth + slot); };
+  const uint32_t x_bar = lay.bar + 8u * kSlots;
+  auto full = [&](int slot) { return lay.bar + 8u * static_cast<uint32_t>(warp * kDepth + slot); };
   Abort ab{&s_abort, p.status};
 
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int i = 0; i < kWarps * kDepth; ++i) mbar_init(base + S::kBarOff + 8u * i, 1);
+    for (int i = 0; i < kSlots; ++i) mbar_init(lay.bar + 8u * i, 1);
     mbar_init(x_bar, 1);
     fence_barrier_init();
   }
-  // the decode table: word 32 v + l holds bf16(level[v >> 4]) (the byte's first
-  // element) in its low half and bf16(level[v & 15]) in its high half
-  uint32_t* const lut = reinterpret_cast<uint32_t*>(gbase + S::kLutOff);
-  for (int i = threadIdx.x; i < kLutWords; i += kThreads) {
-    const int v = i >> 5;
-    lut[i] = static_cast<uint32_t>(c_level_bf16[v >> 4]) | (static_cast<uint32_t>(c_level_bf16[v & 15]) << 16);
+  // the decode table: entry v, lane l holds bf16(level[v >> 4]) (the byte's
+  // first element) in its low half and bf16(level[v & 15]) in its high half;
+  // four lane copies per 16-byte store
+  for (int i = threadIdx.x; i < 256 * 8; i += kThreads) {
+    const int v = i >> 3;
+    const uint32_t w =
+        static_cast<uint32_t>(c_level_bf16[v >> 4]) | (static_cast<uint32_t>(c_level_bf16[v & 15]) << 16);
+    st_shared_v4(lay.lut + static_cast<uint32_t>(v * kLutEntry + (i & 7) * 16), make_uint4(w, w, w, w));
   }
-  // X rows of tokens past M are zero (their MMA columns are never stored)
-  for (int i = threadIdx.x; i < S::kXRows * (kXPitch / 16); i += kThreads) {
-    if (i / (kXPitch / 16) >= p.M) st_shared_v4(base + S::kXOff + static_cast<uint32_t>(i) * 16u, make_uint4(0u, 0u, 0u, 0u));
-  }
+  // the row of zeros read by the lanes of absent tokens
+  for (int i = threadIdx.x; i < kXPitch / 16; i += kThreads)
+    st_shared_v4(lay.x + static_cast<uint32_t>(L::kXRows * kXPitch + i * 16), make_uint4(0u, 0u, 0u, 0u));
   __syncthreads();
 
   if (threadIdx.x == 0) {
@@ -343,62 +368,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t row_bytes = static_cast<uint32_t>(slice_blocks(p, slice) * 128);
     mbar_arrive_expect_tx(x_bar, row_bytes * static_cast<uint32_t>(p.M));
     for (int tok = 0; tok < p.M; ++tok)
-      bulk_load_1d(base + S::kXOff + static_cast<uint32_t>(tok * kXPitch),
+      bulk_load_1d(lay.x + static_cast<uint32_t>(tok * kXPitch),
                    p.X + static_cast<int64_t>(tok) * p.K + slice * (kSliceBlocks * 64), row_bytes, x_bar);
   }
 
-  const uint32_t code_ring = base + S::kCodeOff + static_cast<uint32_t>(warp * kDepth * kCodeSlot);
-  const uint32_t abs_ring = base + S::kAbsOff + static_cast<uint32_t>(warp * kDepth * kAbsSlot);
-  auto issue = [&](const ItemCursor& ic, int slot) {
-    const int g = ic.u % p.groups, s = ic.u / p.groups;
-    const int blk0 = s * kSliceBlocks + ic.it * kItemBlocks;
+  const uint32_t code_ring = lay.ring(warp);
+  const uint32_t abs_ring = lay.abs + static_cast<uint32_t>(warp * kDepth * kAbsSlot);
+  auto issue = [&](int g, int it, int slot) {
+    const int blk0 = slice * kSliceBlocks + it * kItemBlocks;
     mbar_arrive_expect_tx(full(slot), kCodeSlot + kAbsSlot);
     tma_load_2d(code_ring + slot * kCodeSlot, &map_codes, full(slot), blk0 * 32, g * kGroupRows);
     tma_load_2d(abs_ring + slot * kAbsSlot, &map_abs, full(slot), blk0, g * kGroupRows);
   };
+  auto step = [&](int& g, int& it) {
+    if (++it == ipu) {
+      it = 0;
+      ++g;
+    }
+  };
 
-  ItemCursor load_c;
-  load_c.set(p, slice, w_lo);
+  // (group, item) of the item computed and, on lane 0, of the next one to load
+  int cg = w_lo / ipu, cit = w_lo % ipu;
+  int lg = cg, lit = cit;
   if (lane == 0) {
     tma_prefetch_map(&map_codes);
     tma_prefetch_map(&map_abs);
-    ItemCursor ic = load_c;
     for (int q = 0; q < kDepth && q < n_items; ++q) {
-      issue(ic, q);
-      ic.next(p);
+      issue(lg, lit, q);
+      step(lg, lit);
     }
   }
   // every lane acquires the bulk-copied X itself
-  bool ok = mbar_wait_spin(x_bar, 0, ab);
-  const uint32_t lut_lane = base + S::kLutOff + static_cast<uint32_t>(lane) * 4u;
+  bool ok = mbar_wait(x_bar, 0, ab);
+  const uint32_t lut_lane = lay.lut | (static_cast<uint32_t>(lane) << 2);
+  uint32_t x_rows[MT];
+#pragma unroll
+  for (int j = 0; j < MT; ++j)
+    x_rows[j] = lay.x + static_cast<uint32_t>((8 * j + g4 < p.M ? 8 * j + g4 : L::kXRows) * kXPitch);
   float acc[MT][4];
 #pragma unroll
   for (int j = 0; j < MT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
-  ItemCursor cur = load_c;
-  if (lane == 0)
-    for (int q = 0; q < kDepth && q < n_items; ++q) load_c.next(p);   // the lane-0 cursor, kDepth ahead
-  int seg_part = cur.it == 0 ? 0 : 1;   // the current part of a unit
+  int seg_part = cit == 0 ? 0 : 1;   // the current part of a unit
   int k = 0;
+  int slot = 0;
+  uint32_t phase = 0;
   for (; ok && k < n_items; ++k) {
-    const int slot = k % kDepth;
-    if (!__all_sync(0xffffffffu, mbar_wait_spin(full(slot), (k / kDepth) & 1, ab))) {
+    if (!__all_sync(0xffffffffu, mbar_wait(full(slot), phase, ab))) {
       ok = false;
       break;
     }
-    const uint32_t x_row0 = base + S::kXOff + static_cast<uint32_t>(g4 * kXPitch);
-    compute_item<MT>(code_ring + slot * kCodeSlot, abs_ring + slot * kAbsSlot, x_row0, cur.it * kItemBlocks,
-                     lut_lane, g4, t, acc);
+    compute_item<MT>(code_ring + slot * kCodeSlot, abs_ring + slot * kAbsSlot, x_rows, cit * kItemBlocks, lut_lane,
+                     g4, t, acc);
     // the slot's codes have been read by every lane: refill it kDepth items ahead
     __syncwarp();
     if (lane == 0 && k + kDepth < n_items) {
       fence_proxy_async_smem();
-      issue(load_c, slot);
-      load_c.next(p);
+      issue(lg, lit, slot);
+      step(lg, lit);
     }
-    if (cur.it + 1 == unit_items(p, cur.u) || k + 1 == n_items) {
+    if (cit + 1 == ipu || k + 1 == n_items) {
       // the end of this warp's part of the unit (part 0 records whether it is the whole unit)
-      if (seg_part == 0 && lane == 0) p.unit_parts[cur.u] = cur.it + 1 == unit_items(p, cur.u) ? 1 : 2;
-      float* dst = slot_ptr<MT>(p, cur.u, seg_part, lane);
+      const int u = slice * p.groups + cg;
+      if (seg_part == 0 && lane == 0) p.unit_parts[u] = cit + 1 == ipu ? 1 : 2;
+      float* dst = slot_ptr<MT>(p, u, seg_part, lane);
 #pragma unroll
       for (int j = 0; j < MT; ++j) {
         __stcg(reinterpret_cast<float4*>(dst + j * 128), make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]));
@@ -406,13 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       seg_part = 0;
     }
-    cur.next(p);
+    step(cg, cit);
+    if (++slot == kDepth) {
+      slot = 0;
+      phase ^= 1u;
+    }
   }
   if (!ok) {
     // a wait ran out: let the copies this CTA issued land before it exits
     if (lane == 0)
-      for (int q = k; q < n_items && q < k + kDepth; ++q) mbar_wait_spin(full(q % kDepth), (q / kDepth) & 1, ab, false);
-    if (threadIdx.x == 0) mbar_wait_spin(x_bar, 0, ab, false);
+      for (int q = k; q < n_items && q < k + kDepth; ++q) mbar_wait(full(q % kDepth), (q / kDepth) & 1, ab, false);
+    if (threadIdx.x == 0) mbar_wait(x_bar, 0, ab, false);
     return;
   }
 
@@ -428,6 +464,9 @@ __global__ void __launch_bounds__(kFinWarps * 32) lora_stream_finish_kernel(cons
   __shared__ __align__(16) uint8_t b_tile[RP * kFinBPitch];          // B [rp][this CTA's 128 columns]
   __shared__ __align__(16) uint8_t t_tile[16 * (RP * 2 + 16)];       // bf16(s*T) [16 tokens][rp]
   const int n0 = static_cast<int>(blockIdx.x) * kFinCols;
+  // the next call's first kernel may be scheduled now: it waits for this grid
+  // before it touches global memory
+  if (threadIdx.x == 0) griddep_launch_dependents();
   // B is an input of the call: bring this CTA's columns in while the stream kernel finishes
   for (int i = threadIdx.x; i < RP * (kFinCols / 8); i += kFinWarps * 32) {
     const int j = i / (kFinCols / 8), c = (i % (kFinCols / 8)) * 8;
@@ -449,15 +488,29 @@ __global__ void __launch_bounds__(kFinWarps * 32) lora_stream_finish_kernel(cons
   if (g < p.groups) finish_group<MT, RP>(p, g, gw, threadIdx.x & 31, smem_u32(b_tile), smem_u32(t_tile));
 }
 
+// The opt-in shared memory per block less the kernel's static shared memory.
+int stream_dynamic_smem(const void* kern) {
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return -1;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return -1;
+  return optin - static_cast<int>(fa.sharedSizeBytes);
+}
+
 template <int MT>
 cudaError_t launch_stream_mt(const CUtensorMap (&maps)[2], const StreamParams& p, int grid, cudaStream_t stream) {
   auto kern = lora_stream_kernel<MT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, StreamSmem<MT>::kBytes);
+  // all the shared memory a CTA may have: the layout is placed around a 64 KB
+  // boundary of the CTA's window, which the kernel checks it has room for
+  static const int dyn_bytes = stream_dynamic_smem(reinterpret_cast<const void*>(kern));
+  if (dyn_bytes <= 0) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_bytes);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = StreamSmem<MT>::kBytes;
+  cfg.blockDim = dim3(StreamCfg<MT>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = dyn_bytes;
   cfg.stream = stream;
   // programmatic serialisation: the weight stream starts while the rank-r
   // kernel before this one finishes; bf16(s*T) and the counters wait for it

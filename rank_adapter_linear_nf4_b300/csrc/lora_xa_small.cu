@@ -94,9 +94,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kXaThreads, 1
   auto bar = [&](int b) { return base + S::kBarOff + 8u * b; };
   Abort ab{&s_abort, p.status};
 
-  // the token-stream kernel may be scheduled now; it waits for this grid before it reads T
   if (threadIdx.x == 0) {
-    griddep_launch_dependents();
     s_abort = 0;
     for (int b = 0; b < kBufs; ++b) mbar_init(bar(b), 1);
     fence_barrier_init();
@@ -106,6 +104,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kXaThreads, 1
     if ((i / (kXChunkPitch / 16)) % 16 >= p.M)
       st_shared_v4(base + S::kXOff + static_cast<uint32_t>(i) * 16u, make_uint4(0u, 0u, 0u, 0u));
   __syncthreads();
+  // launched with programmatic serialisation, this first kernel of the call may
+  // start while the previous kernel on the stream runs: the set-up above
+  // overlaps it; global memory is touched only after it has completed.  Then
+  // the token-stream kernel may be scheduled (it reads the call's inputs at
+  // once, and waits for this grid before its end, for T).
+  griddep_wait();
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   // this CTA's steps of the contraction, in chunks
   const int steps = p.K / 16;
@@ -220,9 +225,18 @@ cudaError_t launch_xa_rp(const XaParams& p, cudaStream_t stream) {
   auto kern = lora_xa_small_kernel<RP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, XaSmem<RP>::kBytes);
   if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCluster, 1, 1);
+  cfg.blockDim = dim3(kXaThreads, 1, 1);
+  cfg.dynamicSmemBytes = XaSmem<RP>::kBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   LaunchScope scope(kKindRowsT, stream);
-  kern<<<kCluster, kXaThreads, XaSmem<RP>::kBytes, stream>>>(p);
-  return cudaGetLastError();
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 }  // namespace

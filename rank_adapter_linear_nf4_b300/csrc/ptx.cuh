@@ -13,6 +13,7 @@ namespace qlora {
 
 // Status codes written into the device status word (same values as qlora_status).
 constexpr int kStatusTimeout = 6;
+constexpr int kStatusInternal = 8;
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;

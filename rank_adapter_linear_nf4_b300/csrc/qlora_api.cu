@@ -208,6 +208,7 @@ const char* qlora_status_string(qlora_status status) {
     case QLORA_ERR_CUDA: return "QLORA_ERR_CUDA: a CUDA call failed (qlora_last_cuda_error)";
     case QLORA_ERR_TIMEOUT: return "QLORA_ERR_TIMEOUT: a bounded device wait ran out";
     case QLORA_ERR_WORKSPACE: return "QLORA_ERR_WORKSPACE: workspace missing or too small";
+    case QLORA_ERR_INTERNAL: return "QLORA_ERR_INTERNAL: a kernel's shared-memory layout did not fit";
   }
   return "unknown qlora_status";
 }

@@ -20,6 +20,7 @@ STATUS_NAMES = {
     0: "QLORA_OK", 1: "QLORA_ERR_NULL", 2: "QLORA_ERR_SHAPE", 3: "QLORA_ERR_ALIGN",
     4: "QLORA_ERR_UNSUPPORTED", 5: "QLORA_ERR_CUDA", 6: "QLORA_ERR_TIMEOUT",
     7: "QLORA_ERR_WORKSPACE",
+    8: "QLORA_ERR_INTERNAL",
 }
 
 _c_void_p, _i64, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t

@@ -71,3 +71,50 @@ def test_dequant_arbitrary_codes():
                                  n_out, n_in)
     ref = O.dequantize_nf4(packed, absmax, n_out, n_in)
     assert np.array_equal(Wd.cpu().float().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def _all_bf16_upto(m_bits: int) -> np.ndarray:
+    """Every bf16 bit pattern w with |w| <= the positive bf16 m_bits (both signs)."""
+    pos = np.arange(0, m_bits + 1, dtype=np.uint32).astype(np.uint16)
+    return np.concatenate([pos, pos | np.uint16(0x8000)])
+
+
+@pytest.mark.parametrize("m_bits", [0x3F80, 0x3C23, 0x4121, 0x3E9B, 0x0080, 0x0005, 0x7E00, 0x7F7F])
+def test_quantize_every_weight_of_an_absmax(m_bits):
+    """Brute force over the code decision: for one absmax m, every bf16 weight
+    |w| <= m (tens of thousands of values, so every value next to a decision
+    threshold is among them) is quantised in blocks that all hold m, and each
+    code is compared with the oracle's.  The m values cover ordinary scales, the
+    smallest normal and a subnormal bf16, and scales near the top of the range."""
+    vals = _all_bf16_upto(m_bits)
+    per = 63
+    nb = -(-vals.size // per)
+    nb = -(-nb // 64) * 64                               # whole rows of 64 blocks
+    blocks = np.zeros((nb, 64), dtype=np.uint16)
+    blocks[:, 0] = m_bits                                 # absmax of every block is m
+    flat = np.zeros(nb * per, dtype=np.uint16)
+    flat[:vals.size] = vals
+    blocks[:, 1:] = flat.reshape(nb, per)
+    W = torch.from_numpy(blocks.view(np.int16).reshape(nb // 64, 64 * 64)).view(torch.bfloat16)
+    _check_weight(W)
+
+
+# (absmax, weight) bf16 pairs whose quotient lies within 2^-21 of a decision
+# threshold (found by scanning every absmax in [1, 2) and every weight; scaling
+# both by a power of two keeps the quotient): the closest calls the code
+# decision has to make
+_NEAR_PAIRS = [(0x3F83, 0x3ECC), (0x3FA1, 0x3D4D), (0x3FA2, 0xBD6C), (0x3FF3, 0xBDB1)]
+
+
+def test_quantize_weights_next_to_thresholds():
+    rows = []
+    for m_bits, w_bits in _NEAR_PAIRS:
+        for k in (-100, -20, -7, 0, 5, 60, 120):       # both scaled by 2^k
+            blk = np.full(64, (w_bits & 0x7FFF) + (k << 7) | (w_bits & 0x8000), dtype=np.uint16)
+            blk[0] = m_bits + (k << 7)
+            blk[1::2] ^= 0x8000                          # both signs
+            rows.append(blk)
+    blocks = np.stack(rows)
+    blocks = np.concatenate([blocks, np.zeros((64 - len(blocks) % 64, 64), dtype=np.uint16)])
+    W = torch.from_numpy(blocks.view(np.int16).reshape(-1, 64 * 64)).view(torch.bfloat16)
+    _check_weight(W)
