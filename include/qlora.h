@@ -60,7 +60,7 @@ typedef enum qlora_status {
   QLORA_ERR_NULL = 1,         /* a required pointer is NULL */
   QLORA_ERR_SHAPE = 2,        /* a size is negative, zero where not allowed, or too large */
   QLORA_ERR_ALIGN = 3,        /* a device pointer is not 16-byte aligned */
-  QLORA_ERR_UNSUPPORTED = 4,  /* d_in % 64 != 0, d_out % 8 != 0, r outside [1, 128] */
+  QLORA_ERR_UNSUPPORTED = 4,  /* d_in % 64 != 0, d_out % 8 != 0, r outside [1, 256] ([1, 128] for the merge) */
   QLORA_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed; see qlora_last_cuda_error() */
   QLORA_ERR_TIMEOUT = 6,      /* a bounded device-side wait ran out (see qlora_device_status) */
   QLORA_ERR_WORKSPACE = 7,    /* workspace NULL or smaller than qlora_workspace_bytes() */
@@ -192,7 +192,7 @@ size_t qlora_workspace_bytes(int64_t M, int64_t d_in, int64_t d_out, int32_t r);
  *   XA_save  [M, r]     fp32, written: T, needed by qlora_linear_bwd.
  *   workspace / workspace_bytes: caller scratch, >= qlora_workspace_bytes().
  * Requires M >= 0 (M == 0 launches nothing), d_in % 64 == 0, d_out % 8 == 0,
- * 1 <= r <= 128.  Accuracy: fp32 accumulation of bf16 products; the LoRA term
+ * 1 <= r <= 256.  Accuracy: fp32 accumulation of bf16 products; the LoRA term
  * enters the tensor-core accumulator as bf16(s*T) x B.  For 1..16 tokens with
  * d_in % 256 == 0 the weight is streamed by a separate kernel that multiplies
  * bf16(level[q]) by X and applies each block's absmax to the block sum in fp32:
@@ -256,6 +256,39 @@ qlora_status qlora_linear_bwd(const uint16_t* X, const uint16_t* dY,
                               qlora_stream_t stream);
 
 /*
+ * Stacked projections of one input with separate low-rank blocks ("target
+ * modules" of one activation: q/k/v, gate/up; "UnSloth加速原理：CUDA内核融合与内存优化",
+ * section 内核融合).  n_groups projections are one layer whose weight rows are
+ * stacked along d_out (group g owns output features [sum_{i<g} group_d_out[i],
+ * sum_{i<=g} group_d_out[i])) and whose low-rank part is block-diagonal:
+ *   A [d_in, r] with group g in columns [g*group_rank, (g+1)*group_rank),
+ *   B [r, d_out] with group g's block in those rows and its own columns, zero
+ *     elsewhere (the zeros are read: G = dY.B^T runs over all of B),
+ *   r = n_groups * group_rank (zero-padded columns of A give zero rows of dB).
+ * The forward's low-rank term and dB touch only the diagonal blocks: each
+ * output tile adds its own group's T columns times its B block, and dB is
+ * written only in the diagonal blocks (the off-diagonal blocks are left as
+ * they were).  Everything else -- Y, T, dX (summed over the groups), dA --
+ * is qlora_linear_fwd / _bwd with the same A and B.
+ * Requires 1 <= n_groups <= 8, group_rank % 64 == 0, r <= 256, every
+ * group_d_out but the last a multiple of 128, and qlora_linear_fwd's other
+ * requirements with d_out = sum group_d_out; the workspace is
+ * qlora_workspace_bytes(M, d_in, d_out, r).  group_d_out is a host array.
+ */
+qlora_status qlora_linear_fwd_grouped(const uint16_t* X, int64_t M, int64_t d_in, int32_t n_groups,
+                                      const int64_t* group_d_out, int32_t group_rank, const uint8_t* packed,
+                                      const float* absmax, const uint16_t* A, const uint16_t* B, float s,
+                                      uint16_t* Y, float* XA_save, void* workspace, size_t workspace_bytes,
+                                      qlora_stream_t stream);
+
+qlora_status qlora_linear_bwd_grouped(const uint16_t* X, const uint16_t* dY, int64_t M, int64_t d_in,
+                                      int32_t n_groups, const int64_t* group_d_out, int32_t group_rank,
+                                      const uint8_t* packed, const float* absmax, const uint16_t* A,
+                                      const uint16_t* B, float s, const float* XA_saved, uint16_t* dX, float* dA,
+                                      float* dB, void* workspace, size_t workspace_bytes, qlora_stream_t stream);
+
+
+/*
  * SwiGLU MLP block with the gate fused into the layers' epilogues.
  *
  *     gu = X . W_gu_deq^T + s_gu . (X . A_gu) . B_gu      (gate and up projections, one layer)
@@ -313,7 +346,7 @@ size_t qlora_swiglu_mlp_workspace_bytes(int64_t M, int64_t d_model, int64_t d_ff
  *   A_gu [d_model, r_gu], B_gu [r_gu, 2*d_ff] (interleaved columns), s_gu;
  *   down layer: d_packed, d_absmax ([d_model, d_ff] weight), A_d [d_ff, r_d],
  *   B_d [r_d, d_model], s_d.
- * Requires d_model % 64 == 0, d_ff % 64 == 0, ranks in [1, 128]. */
+ * Requires d_model % 64 == 0, d_ff % 64 == 0, ranks in [1, 256]. */
 qlora_status qlora_swiglu_mlp_fwd(const uint16_t* X, int64_t M, int64_t d_model, int64_t d_ff,
                                   const uint8_t* gu_packed, const float* gu_absmax, const uint16_t* A_gu,
                                   const uint16_t* B_gu, int32_t r_gu, float s_gu,

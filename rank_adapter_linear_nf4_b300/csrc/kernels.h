@@ -56,14 +56,33 @@ cudaError_t launch_dequant_nf4(const uint8_t* packed, const float* absmax, int64
 void nf4_levels_host(float out[16]);
 
 // LoRA linear (lora_kernels.cu).
+// Projections stacked along d_out whose low-rank parts stay separate (a
+// block-diagonal B): group g owns output features [end[g-1], end[g]) and rank
+// columns [g * width, (g + 1) * width).  With n == 0 the low-rank part is one
+// dense block.
+constexpr int kMaxLoraGroups = 8;
+struct LoraGroups {
+  int n = 0;
+  int width = 0;                     // a multiple of 64
+  int end[kMaxLoraGroups] = {};      // every end but the last a multiple of 128
+};
+
 struct LayerDims {
   int M;       // tokens
   int K;       // d_in
   int N;       // d_out
   int r;       // LoRA rank
-  int rp;      // r padded to a multiple of 64
+  int rp;      // r padded to 64, 128 or 256 (padded_rank)
   float s;     // LoRA scale
+  LoraGroups groups;   // separate low-rank blocks of stacked projections (forward Y and dB only)
 };
+
+// Largest LoRA rank of a layer call.
+constexpr int kMaxRank = 256;
+
+// The rank padded to a width the rank-r kernels are built for: 64, 128 or 256
+// columns (the tensor-core N of their MMAs, the TMEM columns they allocate).
+inline int padded_rank(int r) { return r <= 64 ? 64 : r <= 128 ? 128 : 256; }
 
 // Workspace carve-up shared by the forward and the backward.
 struct Workspace {

@@ -75,7 +75,7 @@ constexpr int kSkThreads = 192;   // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 
 template <int RP>
 struct SkinnySmem {
-  static constexpr int kStages = RP == 64 ? 8 : 6;   // as many stages as fit: keeps HBM reads in flight
+  static constexpr int kStages = RP == 64 ? 8 : RP == 128 ? 6 : 4;   // as many as fit: keeps HBM reads in flight
   static constexpr int kABytes = kTileP * 128;   // 128 rows x 64 bf16
   static constexpr int kBBytes = RP * 128;       // RP columns x 64 bf16
   static constexpr int kStageBytes = kABytes + kBBytes;
@@ -101,6 +101,9 @@ struct SkinnyParams {
   uint16_t* s_t;       // kRowsG: bf16(s*T) [rows, RP] written from xa
   int* zero;           // rows modes: split-tile counters of the main kernel that follows
   int n_zero;
+  int grp_n;           // kRed job 1 (dB) of stacked projections: only the diagonal blocks,
+  int grp_width;       // grp_width rank rows of group g for the features of g
+  int grp_end[kMaxLoraGroups];
   int wait_first;      // launched with programmatic serialisation as a call's first kernel:
                        // wait for the previous kernel before touching global memory
   int* status;
@@ -161,6 +164,16 @@ __global__ void __launch_bounds__(kSkThreads, 1)
   const int ct_end = static_cast<int>((static_cast<int64_t>(p.num_ct) * (split + 1)) / nsplit);
   const int nct = ct_end - ct_begin;
   Abort ab{&s_abort, p.status};
+  // the low-rank columns this tile contracts against: all of them, or (dB of
+  // stacked projections) the group that owns the tile's features
+  int lr_off = 0, lr_n = RP, lr_valid = p.r;
+  if (MODE == kRed && job == 1 && p.grp_n > 0) {
+    int g = 0;
+    while (g + 1 < p.grp_n && p0 >= p.grp_end[g]) ++g;
+    lr_off = g * p.grp_width;
+    lr_n = p.grp_width;
+    lr_valid = p.grp_width;
+  }
 
   if (threadIdx.x == 0) {
     // a dependent kernel may be scheduled now: it waits (griddepcontrol.wait)
@@ -208,7 +221,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         const uint32_t a = base + slot * S::kStageBytes;
         const uint32_t b = a + S::kABytes;
         const uint32_t full = bar0 + 8u * slot;
-        mbar_arrive_expect_tx(full, S::kStageBytes);
+        mbar_arrive_expect_tx(full, kBmn ? S::kABytes + (lr_n / 64) * 8192 : S::kStageBytes);
         if (kAmn) {
           tma_load_2d(a, map_a, full, p0, ct * kTileK);
           tma_load_2d(a + 8192, map_a, full, p0 + 64, ct * kTileK);
@@ -217,7 +230,8 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         }
         if (kBmn) {
 #pragma unroll
-          for (int jb = 0; jb < RP / 64; ++jb) tma_load_2d(b + jb * 8192, map_b, full, jb * 64, ct * kTileK);
+          for (int jb = 0; jb < RP / 64; ++jb)
+            if (jb * 64 < lr_n) tma_load_2d(b + jb * 8192, map_b, full, lr_off + jb * 64, ct * kTileK);
         } else {
           tma_load_2d(b, map_b, full, ct * kTileK, 0);
         }
@@ -228,7 +242,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = umma_idesc_bf16(kTileP, RP, kAmn ? 1 : 0, kBmn ? 1 : 0);
+      const uint32_t idesc = umma_idesc_bf16(kTileP, lr_n, kAmn ? 1 : 0, kBmn ? 1 : 0);
       for (int i = 0; i < nct; ++i) {
         const int slot = i % S::kStages;
         const uint32_t ph = (i / S::kStages) & 1;
@@ -334,7 +348,7 @@ __global__ void __launch_bounds__(kSkThreads, 1)
         } else {
 #pragma unroll
           for (int c = 0; c < 4; ++c)
-            if (col + c < p.r) j_out_f32[static_cast<int64_t>(col + c) * j_rows + grow] = vals[c];
+            if (col + c < lr_valid) j_out_f32[static_cast<int64_t>(lr_off + col + c) * j_rows + grow] = vals[c];
         }
       }
     }
@@ -444,6 +458,11 @@ struct MainParams {
   int sk_tiles;            // tiles dp_tiles .. dp_tiles + sk_tiles - 1 are split
   int sk_ctas;             // CTAs sharing the split remainder
   int debug_stall;         // test hook: the token producer issues nothing, so every wait runs out
+  // Y of stacked projections with separate low-rank blocks: the tile at output
+  // feature p0 runs the LoRA stages of its group, starting at stage grp_lt0 * g
+  int grp_n;
+  int grp_lt0;
+  int grp_end[kMaxLoraGroups];
   // SwiGLU gate fused into the epilogue (rows of W and columns of the output
   // interleaved in 64-row chunks: [gate 0..63 | up 0..63 | gate 64..127 | ...]):
   //   Y (gate_fwd):  besides gu = the layer's output, h = silu(g) * u via map_h;
@@ -650,7 +669,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
               griddep_launch_dependents();
               lora_ready = true;
             }
-            const int j = s - p.num_kt;
+            int j = s - p.num_kt;
+            if (!kTrans && p.grp_n > 0) {
+              int g = 0;
+              while (g + 1 < p.grp_n && p0 >= p.grp_end[g]) ++g;
+              j += g * p.grp_lt0;
+            }
             mbar_arrive_expect_tx(full(slot), S::kActBytes + S::kWBytes);
 #pragma unroll
             for (int h = 0; h < S::kHalves; ++h)
@@ -1153,7 +1177,8 @@ template <int MODE>
 cudaError_t launch_skinny(int rp, const CUtensorMap (&maps)[4], const SkinnyParams& sp, int tiles,
                           int split, cudaStream_t stream, bool pdl = false) {
   if (rp == 64) return launch_skinny_split<MODE, 64>(maps, sp, tiles, split, pdl, stream);
-  return launch_skinny_split<MODE, 128>(maps, sp, tiles, split, pdl, stream);
+  if (rp == 128) return launch_skinny_split<MODE, 128>(maps, sp, tiles, split, pdl, stream);
+  return launch_skinny_split<MODE, 256>(maps, sp, tiles, split, pdl, stream);
 }
 
 // Split-remainder buffers the main kernel may use (from the workspace).
@@ -1287,6 +1312,14 @@ cudaError_t launch_main(const LayerDims& d, const uint16_t* act, const uint16_t*
   mp.N = d.N;
   mp.num_kt = (C + kTileK - 1) / kTileK;
   mp.num_lt = d.rp / kTileK;
+  mp.grp_n = 0;
+  mp.grp_lt0 = 0;
+  if (!kTrans && d.groups.n > 0) {
+    mp.grp_n = d.groups.n;
+    mp.grp_lt0 = d.groups.width / kTileK;
+    mp.num_lt = mp.grp_lt0;
+    for (int g = 0; g < kMaxLoraGroups; ++g) mp.grp_end[g] = d.groups.end[g];
+  }
   mp.debug_stall = take_debug_stall() ? 1 : 0;
   mp.status = status;
   const SplitBuffers sb = {ws.partials, ws.partial_bytes, ws.counters, ws.counter_cap};
@@ -1465,6 +1498,12 @@ cudaError_t run_backward(const LayerDims& d, const uint16_t* X, const uint16_t* 
     sp.job[0].rows = d.K;
     sp.job[0].tiles = (d.K + kTileP - 1) / kTileP;
     sp.job[0].out_f32 = dA;
+    if (d.groups.n > 0) {
+      // stacked projections: dB only in the diagonal blocks
+      sp.grp_n = d.groups.n;
+      sp.grp_width = d.groups.width;
+      for (int g = 0; g < kMaxLoraGroups; ++g) sp.grp_end[g] = d.groups.end[g];
+    }
     sp.job[1].rows = d.N;
     sp.job[1].tiles = (d.N + kTileP - 1) / kTileP;
     sp.job[1].out_f32 = dB;

@@ -16,6 +16,7 @@
 //     qlora_dequant_nf4, so W_deq is that kernel's output bit for bit -- rounds
 //     once to bf16, out = bf16_rn(fma(s, D, W_deq)), stages the tile in the
 //     operands' shared memory (128-byte swizzle) and writes it with TMA stores.
+#include <algorithm>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -199,6 +200,234 @@ __global__ void __launch_bounds__(kMergeThreads) lora_merge_kernel(const __grid_
   }
 }
 
+// ---------------------------------------------------------------------------
+// Persistent form (r % 8 == 0, A and B 16-byte aligned): one CTA per SM takes
+// a contiguous run of 128 x 128 output tiles in row-block order, so its B^T
+// operand is loaded once per row block.  Warp 16 (one lane) loads A^T tiles by
+// TMA into a two-slot ring and issues each tile's rank-r MMA into one of two
+// TMEM accumulators; warps 0-15 are the epilogue (TMEM lane = tile row; warps
+// w, w + 4, w + 8, w + 12 take 32 columns each): while tile i's MMA runs they
+// finish tile i - 1 -- its codes and absmax were loaded from global memory two
+// tiles ahead -- into one of two staging buffers, which a TMA store writes out
+// while the next tile is computed.
+constexpr int kMpEpiWarps = 16;
+constexpr int kMpThreads = (kMpEpiWarps + 1) * 32;
+constexpr int kMpASlots = 2;
+
+template <int RP>
+struct MergePSmem {
+  static constexpr int kChunks = RP / 64;
+  static constexpr int kOpBytes = kChunks * 16384;            // one operand (B^T or an A^T tile)
+  static constexpr int kBtOff = 0;
+  static constexpr int kAOff = kBtOff + kOpBytes;
+  static constexpr int kStageOff = kAOff + kMpASlots * kOpBytes;   // two 32 KB output stagings
+  static constexpr int kBarOff = kStageOff + 2 * 32768;
+  // bars: a_full[2], a_empty[2], tmem_full[2], tmem_empty[2], bt_full, bt_free, drain
+  static constexpr int kBytes = kBarOff + 8 * 11 + 1024;
+};
+
+template <int RP>
+__global__ void __launch_bounds__(kMpThreads, 1)
+    lora_merge_persistent_kernel(const __grid_constant__ CUtensorMap map_out,   // W_out [N, K] bf16, box {64, 128}
+                                 const __grid_constant__ CUtensorMap map_a,     // A [K, r] bf16, box {64, 128}, SW128
+                                 const __grid_constant__ CUtensorMap map_b,     // B [r, N] bf16, box {64, 64}, SW128
+                                 const MergeParams p, int k_tiles, int tiles) {
+  using S = MergePSmem<RP>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ int s_abort;
+  __shared__ uint32_t s_tmem;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t bars = base + S::kBarOff;
+  auto a_full = [&](int s) { return bars + 8u * s; };
+  auto a_empty = [&](int s) { return bars + 16u + 8u * s; };
+  auto tmem_full = [&](int b) { return bars + 32u + 8u * b; };
+  auto tmem_empty = [&](int b) { return bars + 48u + 8u * b; };
+  const uint32_t bt_full = bars + 64u, bt_free = bars + 72u, drain = bars + 80u;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  Abort ab{&s_abort, p.status};
+  // this CTA's tiles: [t_begin, t_end) of the row-block-major order
+  const int t_begin = static_cast<int>(static_cast<int64_t>(tiles) * blockIdx.x / gridDim.x);
+  const int t_end = static_cast<int>(static_cast<int64_t>(tiles) * (blockIdx.x + 1) / gridDim.x);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < kMpASlots; ++s) {
+      mbar_init(a_full(s), 1);
+      mbar_init(a_empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tmem_full(b), 1);
+      mbar_init(tmem_empty(b), kMpEpiWarps);
+    }
+    mbar_init(bt_full, 1);
+    mbar_init(bt_free, 1);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(&s_tmem), 256);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == kMpEpiWarps) {
+    // ---------------- A^T / B^T loads and the MMAs (one lane)
+    if (lane == 0) {
+      tma_prefetch_map(&map_a);
+      tma_prefetch_map(&map_b);
+      tma_prefetch_map(&map_out);
+      auto load_a = [&](int tile, int slot) {
+        const int k0 = (tile % k_tiles) * kMergeTile;
+        mbar_arrive_expect_tx(a_full(slot), S::kOpBytes);
+#pragma unroll
+        for (int c = 0; c < S::kChunks; ++c)
+          tma_load_2d(base + S::kAOff + slot * S::kOpBytes + c * 16384, &map_a, a_full(slot), c * 64, k0);
+      };
+      auto load_bt = [&](int nb) {
+        const int n0 = nb * kMergeTile;
+        mbar_arrive_expect_tx(bt_full, S::kOpBytes);
+#pragma unroll
+        for (int c = 0; c < S::kChunks; ++c)
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(base + S::kBtOff + c * 16384 + h * 8192, &map_b, bt_full, n0 + 64 * h, c * 64);
+      };
+      int loaded = 0;   // A tiles requested (relative to t_begin)
+      for (; loaded < kMpASlots && t_begin + loaded < t_end; ++loaded) load_a(t_begin + loaded, loaded);
+      constexpr uint32_t idesc = umma_idesc_bf16(kMergeTile, kMergeTile, 1, 0);
+      int nb_loaded = -1, bt_loads = 0, bt_frees = 0;
+      int i = 0;   // A tiles consumed
+      for (int tile = t_begin; tile < t_end; ++i, ++tile) {
+        const int nb = tile / k_tiles, slot = i % kMpASlots, buf = i & 1;
+        if (nb != nb_loaded) {
+          if (bt_loads > 0) {
+            // the MMAs that read the previous B^T must have completed
+            umma_commit(bt_free);
+            if (!mbar_wait(bt_free, bt_frees & 1, ab)) break;
+            ++bt_frees;
+          }
+          load_bt(nb);
+          if (!mbar_wait(bt_full, bt_loads & 1, ab)) break;
+          ++bt_loads;
+          nb_loaded = nb;
+        }
+        if (!mbar_wait(a_full(slot), (i / kMpASlots) & 1, ab)) break;
+        if (!mbar_wait(tmem_empty(buf), ((i >> 1) & 1) ^ 1, ab)) {
+          ++i;   // this tile's copy has landed
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d = tmem + static_cast<uint32_t>(buf * kMergeTile);
+#pragma unroll
+        for (int c = 0; c < S::kChunks; ++c) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = sw128_desc(base + S::kBtOff + c * 16384 + kk * 2048, 8192, 1024);
+            const uint64_t bd = sw128_desc(base + S::kAOff + slot * S::kOpBytes + c * 16384 + kk * 32, 16, 1024);
+            umma_bf16(d, ad, bd, idesc, (c | kk) != 0 ? 1u : 0u);
+          }
+        }
+        umma_commit(a_empty(slot));
+        umma_commit(tmem_full(buf));
+        // refill the slot for the tile kMpASlots ahead once these MMAs have read it
+        if (t_begin + loaded < t_end) {
+          if (!mbar_wait(a_empty(slot), (i / kMpASlots) & 1, ab)) {
+            ++i;
+            break;
+          }
+          load_a(t_begin + loaded, slot);
+          ++loaded;
+        }
+      }
+      // after a wait ran out: let the A copies still in flight land
+      for (int q = i; q < loaded; ++q) mbar_wait(a_full(q % kMpASlots), (q / kMpASlots) & 1, ab, false);
+      // every MMA issued here has completed before TMEM is released
+      umma_commit(drain);
+      mbar_wait(drain, 0, ab, false);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue: row i of the tile, columns 32*q .. 32*q+31
+    const int quarter = warp & 3, q = warp >> 2;
+    const int i = quarter * 32 + lane;
+    const int kblocks = p.K >> 6;
+    // codes (16 B) and absmax of tile `tile` for this thread, zero outside the matrix
+    auto fetch = [&](int tile, uint4& c, float& am) {
+      c = make_uint4(0u, 0u, 0u, 0u);
+      am = 0.0f;
+      if (tile >= t_end) return;
+      const int n = (tile / k_tiles) * kMergeTile + i, k = (tile % k_tiles) * kMergeTile + 32 * q;
+      if (n >= p.N || k >= p.K) return;
+      c = ldg_nc_v4(p.packed + static_cast<int64_t>(n) * (p.K / 2) + k / 2);
+      am = ldg_nc_f32(p.absmax + static_cast<int64_t>(n) * kblocks + (k >> 6));
+    };
+    // two tiles ahead
+    uint4 c0, c1, c2;
+    float a0, a1, a2;
+    fetch(t_begin, c0, a0);
+    fetch(t_begin + 1, c1, a1);
+    for (int it = 0, tile = t_begin; tile < t_end; ++it, ++tile) {
+      const int buf = it & 1;
+      fetch(tile + 2, c2, a2);
+      // every epilogue warp runs every iteration and meets both named barriers,
+      // whether or not a wait ran out (then it only skips the work)
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(tmem_full(buf), (it >> 1) & 1, ab));
+      uint32_t v[32];
+      if (ok) {
+        tc_fence_after_sync();
+        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * kMergeTile + 32 * q, v);
+        tmem_ld_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tmem_empty(buf));
+      }
+      // the staging buffer of this tile was last stored two tiles ago
+      if (threadIdx.x == 0) tma_store_wait_read_le1();
+      named_bar_sync(1, kMpEpiWarps * 32);
+      if (ok) {
+        const Nf4BlockTable tab = nf4_block_table(a0);
+        const uint32_t words[4] = {c0.x, c0.y, c0.z, c0.w};
+        // staging: two [128 rows][64 columns] halves, 128-byte swizzled rows
+        const uint32_t row = base + S::kStageOff + buf * 32768u + static_cast<uint32_t>(q >> 1) * 16384u +
+                             static_cast<uint32_t>(i) * 128u;
+#pragma unroll
+        for (int wq = 0; wq < 4; ++wq) {
+          const uint4 wd = nf4_expand8(words[wq], tab);   // elements 8wq..8wq+7 of the thread's 32
+          const uint32_t pr[4] = {wd.x, wd.y, wd.z, wd.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float w0 = __uint_as_float(pr[e] << 16), w1 = __uint_as_float(pr[e] & 0xFFFF0000u);
+            o[e] = pack_bf16x2(fmaf(p.s, __uint_as_float(v[8 * wq + 2 * e]), w0),
+                               fmaf(p.s, __uint_as_float(v[8 * wq + 2 * e + 1]), w1));
+          }
+          const uint32_t chunk = static_cast<uint32_t>((q & 1) * 4 + wq);   // 16-B chunk of the 128-B row
+          st_shared_v4(row + ((chunk ^ static_cast<uint32_t>(i & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+        }
+        fence_proxy_async_smem();
+      }
+      named_bar_sync(1, kMpEpiWarps * 32);
+      if (threadIdx.x == 0 && s_abort == 0) {
+        const int n0 = (tile / k_tiles) * kMergeTile, k0 = (tile % k_tiles) * kMergeTile;
+        tma_store_2d(&map_out, base + S::kStageOff + buf * 32768u, k0, n0);
+        if (k0 + 64 < p.K) tma_store_2d(&map_out, base + S::kStageOff + buf * 32768u + 16384u, k0 + 64, n0);
+        tma_store_commit();
+      }
+      c0 = c1;
+      a0 = a1;
+      c1 = c2;
+      a1 = a2;
+    }
+    if (threadIdx.x == 0) tma_store_wait_all();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
 template <int RP>
 cudaError_t launch_merge_rp(const CUtensorMap& map_out, const MergeParams& mp, cudaStream_t stream) {
   auto kern = lora_merge_kernel<RP>;
@@ -207,6 +436,23 @@ cudaError_t launch_merge_rp(const CUtensorMap& map_out, const MergeParams& mp, c
   const dim3 grid((mp.K + kMergeTile - 1) / kMergeTile, (mp.N + kMergeTile - 1) / kMergeTile);
   LaunchScope scope(kKindMerge, stream);
   kern<<<grid, kMergeThreads, MergeSmem<RP>::kBytes, stream>>>(map_out, mp);
+  return cudaGetLastError();
+}
+
+template <int RP>
+cudaError_t launch_merge_persistent_rp(const CUtensorMap (&maps)[3], const MergeParams& mp, cudaStream_t stream) {
+  auto kern = lora_merge_persistent_kernel<RP>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, MergePSmem<RP>::kBytes);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int k_tiles = (mp.K + kMergeTile - 1) / kMergeTile;
+  const int tiles = k_tiles * ((mp.N + kMergeTile - 1) / kMergeTile);
+  const int grid = std::min(tiles, sms);
+  LaunchScope scope(kKindMerge, stream);
+  kern<<<grid, kMpThreads, MergePSmem<RP>::kBytes, stream>>>(maps[0], maps[1], maps[2], mp, k_tiles, tiles);
   return cudaGetLastError();
 }
 
@@ -230,6 +476,20 @@ cudaError_t launch_merge_nf4(const uint8_t* packed, const float* absmax, int N, 
   mp.a_vec = (reinterpret_cast<uintptr_t>(A) % 16 == 0 && r % 8 == 0) ? 1 : 0;
   mp.b_vec = (reinterpret_cast<uintptr_t>(B) % 16 == 0) ? 1 : 0;
   mp.status = status;
+  if (mp.a_vec && mp.b_vec) {
+    // A^T and B^T tiles by TMA: rows of A are r * 2 bytes (a multiple of 16 when r % 8 == 0)
+    CUtensorMap maps[3];
+    maps[0] = map_out;
+    if (!make_tensor_map_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, static_cast<uint64_t>(r),
+                            static_cast<uint64_t>(K), static_cast<uint64_t>(r) * 2, 64, kMergeTile,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, static_cast<uint64_t>(N),
+                            static_cast<uint64_t>(r), static_cast<uint64_t>(N) * 2, 64, 64,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    if (r <= 64) return launch_merge_persistent_rp<64>(maps, mp, stream);
+    return launch_merge_persistent_rp<128>(maps, mp, stream);
+  }
   if (r <= 64) return launch_merge_rp<64>(map_out, mp, stream);
   return launch_merge_rp<128>(map_out, mp, stream);
 }

@@ -94,7 +94,7 @@ struct StreamCfg {
 template <int MT>
 struct StreamLayout {
   static constexpr int kSlots = StreamCfg<MT>::kSlots;
-  static constexpr int kXRows = 8 * MT;   // token rows of the X slice, then one row of zeros
+  static constexpr int kXRows = 8 * MT;   // token rows of the X slice
   uint32_t code_lo, n_lo;   // slots 0 .. n_lo-1 below the table
   uint32_t lut;
   uint32_t code_hi;         // slots n_lo .. kSlots-1 above it
@@ -108,7 +108,7 @@ struct StreamLayout {
     code_hi = lut + kLutBytes;
     abs = code_hi + (kSlots - n_lo) * kCodeSlot;
     x = abs + kSlots * kAbsSlot;
-    bar = x + (kXRows + 1) * kXPitch;
+    bar = x + kXRows * kXPitch;
     end = bar + 8u * (kSlots + 1);
   }
   __device__ __forceinline__ uint32_t ring(int warp) const {
@@ -163,6 +163,19 @@ __device__ __forceinline__ uint32_t lut_pair(uint32_t lut_lane, uint32_t w, uint
   return lds32(prmt(w, lut_lane, sel));
 }
 
+// 16 bytes of shared memory if `on`, else zeros.
+__device__ __forceinline__ uint4 ld_shared_v4_if(uint32_t addr, bool on) {
+  uint4 v;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %5, 0;\n\t"
+      "mov.u32 %0, 0;\n\tmov.u32 %1, 0;\n\tmov.u32 %2, 0;\n\tmov.u32 %3, 0;\n\t"
+      "@p ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "r"(addr), "r"(static_cast<uint32_t>(on)));
+  return v;
+}
+
 // Blocks of slice s.
 __device__ __forceinline__ int slice_blocks(const StreamParams& p, int s) {
   return min(kSliceBlocks, p.kb - s * kSliceBlocks);
@@ -179,12 +192,11 @@ struct SliceSplit {
   __device__ __forceinline__ static int active_warps(int n_cta) { return min(W, max(1, n_cta / kItemBlocks)); }
 };
 
-// One item's MMAs: acc += absmax * (codes of 16 rows x 4 blocks) . X.  Lanes
-// of token rows at or past M read the row of zeros (one address for all of
-// them; their MMA columns are never stored).
+// One item's MMAs: acc += absmax * (codes of 16 rows x 4 blocks) . X.  Token
+// rows at or past M are not read (their MMA columns are never stored).
 template <int MT>
-__device__ __forceinline__ void compute_item(uint32_t code_slot, uint32_t abs_slot, const uint32_t (&x_rows)[MT],
-                                             int blk0, uint32_t lut_lane, int g4, int t, float (&acc)[MT][4]) {
+__device__ __forceinline__ void compute_item(uint32_t code_slot, uint32_t abs_slot, uint32_t x_row0, int blk0,
+                                             uint32_t lut_lane, int g4, int t, int M, float (&acc)[MT][4]) {
   const uint32_t ra = static_cast<uint32_t>(g4), rb = static_cast<uint32_t>(g4 + 8);
   const uint4 am_a4 = ld_shared_v4(abs_slot + ra * 16u);   // the item's four block scales, rows g and g+8
   const uint4 am_b4 = ld_shared_v4(abs_slot + rb * 16u);
@@ -201,9 +213,11 @@ __device__ __forceinline__ void compute_item(uint32_t code_slot, uint32_t abs_sl
     uint4 x[MT][2];
 #pragma unroll
     for (int j = 0; j < MT; ++j) {
-      const uint32_t src = x_rows[j] + static_cast<uint32_t>(((blk0 + blk) * 64 + 16 * t) * 2);
-      x[j][0] = ld_shared_v4(src);
-      x[j][1] = ld_shared_v4(src + 16);
+      const uint32_t src = x_row0 + static_cast<uint32_t>(j * 8 * kXPitch) +
+                           static_cast<uint32_t>(((blk0 + blk) * 64 + 16 * t) * 2);
+      const bool live = 8 * j + g4 < M;
+      x[j][0] = ld_shared_v4_if(src, live);
+      x[j][1] = ld_shared_v4_if(src + 16, live);
     }
     float d[MT][4];
 #pragma unroll
@@ -358,9 +372,6 @@ __global__ void __launch_bounds__(StreamCfg<MT>::kThreads, 1)
         static_cast<uint32_t>(c_level_bf16[v >> 4]) | (static_cast<uint32_t>(c_level_bf16[v & 15]) << 16);
     st_shared_v4(lay.lut + static_cast<uint32_t>(v * kLutEntry + (i & 7) * 16), make_uint4(w, w, w, w));
   }
-  // the row of zeros read by the lanes of absent tokens
-  for (int i = threadIdx.x; i < kXPitch / 16; i += kThreads)
-    st_shared_v4(lay.x + static_cast<uint32_t>(L::kXRows * kXPitch + i * 16), make_uint4(0u, 0u, 0u, 0u));
   __syncthreads();
 
   if (threadIdx.x == 0) {
@@ -401,10 +412,7 @@ __global__ void __launch_bounds__(StreamCfg<MT>::kThreads, 1)
   // every lane acquires the bulk-copied X itself
   bool ok = mbar_wait(x_bar, 0, ab);
   const uint32_t lut_lane = lay.lut | (static_cast<uint32_t>(lane) << 2);
-  uint32_t x_rows[MT];
-#pragma unroll
-  for (int j = 0; j < MT; ++j)
-    x_rows[j] = lay.x + static_cast<uint32_t>((8 * j + g4 < p.M ? 8 * j + g4 : L::kXRows) * kXPitch);
+  const uint32_t x_row0 = lay.x + static_cast<uint32_t>(g4 * kXPitch);
   float acc[MT][4];
 #pragma unroll
   for (int j = 0; j < MT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
@@ -417,8 +425,8 @@ __global__ void __launch_bounds__(StreamCfg<MT>::kThreads, 1)
       ok = false;
       break;
     }
-    compute_item<MT>(code_ring + slot * kCodeSlot, abs_ring + slot * kAbsSlot, x_rows, cit * kItemBlocks, lut_lane,
-                     g4, t, acc);
+    compute_item<MT>(code_ring + slot * kCodeSlot, abs_ring + slot * kAbsSlot, x_row0, cit * kItemBlocks, lut_lane,
+                     g4, t, p.M, acc);
     // the slot's codes have been read by every lane: refill it kDepth items ahead
     __syncwarp();
     if (lane == 0 && k + kDepth < n_items) {
@@ -563,7 +571,7 @@ size_t stream_partial_bytes(const LayerDims& d, int sms) {
 // The absmax rows are read by TMA in 16-byte boxes, and an item is four blocks:
 // K a multiple of 256; and there must be a CTA for every slice.
 bool stream_applies(const LayerDims& d, const Workspace& ws, int sms) {
-  if (d.M < 1 || d.M > kStreamMaxTokens || d.K % 256 != 0) return false;
+  if (d.M < 1 || d.M > kStreamMaxTokens || d.K % 256 != 0 || d.rp > 128) return false;
   if ((d.K / 64 + kSliceBlocks - 1) / kSliceBlocks > sms - kStreamReservedSms) return false;
   if (ws.partials == nullptr) return false;
   return ws.partial_bytes >= stream_partial_bytes(d, sms);

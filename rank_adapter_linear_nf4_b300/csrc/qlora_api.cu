@@ -64,7 +64,7 @@ qlora_status check_codec_shape(int64_t n_out, int64_t n_in) {
 qlora_status check_layer(int64_t M, int64_t d_in, int64_t d_out, int32_t r) {
   if (M < 0 || d_in < 1 || d_out < 1) return QLORA_ERR_SHAPE;
   if (M > kMaxDim || d_in > kMaxDim || d_out > kMaxDim) return QLORA_ERR_SHAPE;
-  if (d_in % 64 != 0 || d_out % 8 != 0 || r < 1 || r > 128) return QLORA_ERR_UNSUPPORTED;
+  if (d_in % 64 != 0 || d_out % 8 != 0 || r < 1 || r > qlora::kMaxRank) return QLORA_ERR_UNSUPPORTED;
   return QLORA_OK;
 }
 
@@ -74,7 +74,7 @@ qlora::LayerDims dims_of(int64_t M, int64_t d_in, int64_t d_out, int32_t r, floa
   d.K = static_cast<int>(d_in);
   d.N = static_cast<int>(d_out);
   d.r = r;
-  d.rp = (r + 63) / 64 * 64;
+  d.rp = qlora::padded_rank(r);
   d.s = s;
   return d;
 }
@@ -358,6 +358,98 @@ qlora_status qlora_linear_bwd(const uint16_t* X, const uint16_t* dY, int64_t M, 
     return QLORA_ERR_ALIGN;
   const qlora::LayerDims d = dims_of(M, d_in, d_out, r, s);
   if (workspace == nullptr || workspace_bytes < qlora::workspace_bytes(d)) return QLORA_ERR_WORKSPACE;
+  int* status = nullptr;
+  st = status_word(&status);
+  if (st != QLORA_OK) return st;
+  cudaError_t e = qlora::run_backward(d, X, dY, packed, absmax, A, B, XA_saved, dX, dA, dB,
+                                      qlora::carve_workspace(d, workspace), status, cs);
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+// ---------------------------------------------------------------- stacked projections, separate low-rank blocks
+
+namespace {
+// Group layout of a stacked layer; fills d_out and the kernels' LoraGroups.
+qlora_status check_groups(int32_t n_groups, const int64_t* group_d_out, int32_t group_rank, int64_t* d_out,
+                          qlora::LoraGroups* g) {
+  if (group_d_out == nullptr) return QLORA_ERR_NULL;
+  if (n_groups < 1 || n_groups > qlora::kMaxLoraGroups || group_rank < 1) return QLORA_ERR_UNSUPPORTED;
+  if (group_rank % 64 != 0 || static_cast<int64_t>(n_groups) * group_rank > qlora::kMaxRank)
+    return QLORA_ERR_UNSUPPORTED;
+  int64_t end = 0;
+  *g = qlora::LoraGroups{};
+  g->n = n_groups;
+  g->width = group_rank;
+  for (int i = 0; i < n_groups; ++i) {
+    if (group_d_out[i] < 1 || group_d_out[i] > kMaxDim) return QLORA_ERR_SHAPE;
+    if (i + 1 < n_groups && group_d_out[i] % 128 != 0) return QLORA_ERR_UNSUPPORTED;
+    end += group_d_out[i];
+    if (end > kMaxDim) return QLORA_ERR_SHAPE;
+    g->end[i] = static_cast<int>(end);
+  }
+  *d_out = end;
+  return QLORA_OK;
+}
+}  // namespace
+
+qlora_status qlora_linear_fwd_grouped(const uint16_t* X, int64_t M, int64_t d_in, int32_t n_groups,
+                                      const int64_t* group_d_out, int32_t group_rank, const uint8_t* packed,
+                                      const float* absmax, const uint16_t* A, const uint16_t* B, float s,
+                                      uint16_t* Y, float* XA_save, void* workspace, size_t workspace_bytes,
+                                      qlora_stream_t stream) {
+  int64_t d_out = 0;
+  qlora::LoraGroups groups;
+  qlora_status st = check_groups(n_groups, group_d_out, group_rank, &d_out, &groups);
+  if (st != QLORA_OK) return st;
+  const int32_t r = n_groups * group_rank;
+  st = check_layer(M, d_in, d_out, r);
+  if (st != QLORA_OK) return st;
+  if (!packed || !absmax || !A || !B) return QLORA_ERR_NULL;
+  if (M == 0) return QLORA_OK;
+  if (!X || !Y || !XA_save) return QLORA_ERR_NULL;
+  if (!aligned16(X) || !aligned16(packed) || !aligned16(absmax) || !aligned16(A) || !aligned16(B) ||
+      !aligned16(Y) || !aligned16(XA_save) || !aligned16(workspace))
+    return QLORA_ERR_ALIGN;
+  qlora::LayerDims d = dims_of(M, d_in, d_out, r, s);
+  if (workspace == nullptr || workspace_bytes < qlora::workspace_bytes(d)) return QLORA_ERR_WORKSPACE;
+  d.groups = groups;
+  int* status = nullptr;
+  st = status_word(&status);
+  if (st != QLORA_OK) return st;
+  cudaError_t e = qlora::run_forward(d, X, packed, absmax, A, B, Y, XA_save, qlora::carve_workspace(d, workspace),
+                                     status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+qlora_status qlora_linear_bwd_grouped(const uint16_t* X, const uint16_t* dY, int64_t M, int64_t d_in,
+                                      int32_t n_groups, const int64_t* group_d_out, int32_t group_rank,
+                                      const uint8_t* packed, const float* absmax, const uint16_t* A,
+                                      const uint16_t* B, float s, const float* XA_saved, uint16_t* dX, float* dA,
+                                      float* dB, void* workspace, size_t workspace_bytes, qlora_stream_t stream) {
+  int64_t d_out = 0;
+  qlora::LoraGroups groups;
+  qlora_status st = check_groups(n_groups, group_d_out, group_rank, &d_out, &groups);
+  if (st != QLORA_OK) return st;
+  const int32_t r = n_groups * group_rank;
+  st = check_layer(M, d_in, d_out, r);
+  if (st != QLORA_OK) return st;
+  if (!packed || !absmax || !A || !B || !dA || !dB) return QLORA_ERR_NULL;
+  if (!aligned16(packed) || !aligned16(absmax) || !aligned16(A) || !aligned16(B) || !aligned16(dA) ||
+      !aligned16(dB))
+    return QLORA_ERR_ALIGN;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (M == 0) {
+    cudaError_t e = cudaMemsetAsync(dA, 0, sizeof(float) * static_cast<size_t>(d_in) * r, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dB, 0, sizeof(float) * static_cast<size_t>(d_out) * r, cs);
+    return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+  }
+  if (!X || !dY || !XA_saved) return QLORA_ERR_NULL;
+  if (!aligned16(X) || !aligned16(dY) || !aligned16(XA_saved) || !aligned16(workspace) ||
+      (dX != nullptr && !aligned16(dX)))
+    return QLORA_ERR_ALIGN;
+  qlora::LayerDims d = dims_of(M, d_in, d_out, r, s);
+  if (workspace == nullptr || workspace_bytes < qlora::workspace_bytes(d)) return QLORA_ERR_WORKSPACE;
+  d.groups = groups;
   int* status = nullptr;
   st = status_word(&status);
   if (st != QLORA_OK) return st;

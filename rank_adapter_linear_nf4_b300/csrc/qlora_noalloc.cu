@@ -82,7 +82,7 @@ extern "C" qlora_status qlora_linear_fwd_noalloc(const uint16_t* X, int64_t M, i
   d.K = static_cast<int>(d_in);
   d.N = static_cast<int>(d_out);
   d.r = r;
-  d.rp = (r + 63) / 64 * 64;
+  d.rp = qlora::padded_rank(r);
   d.s = s;
   // the forward reads and writes bf16(s*T) [M, rp] and, only for ranks whose
   // rows are not 16-byte multiples (r % 8 != 0), a zero-padded copy of A [d_in, rp]

@@ -70,6 +70,13 @@ _SIGNATURES = {
                                         _c_void_p, _c_void_p, _c_void_p, _i32, _f32, _c_void_p,
                                         _c_void_p, _c_void_p, _c_void_p, _c_void_p, _sz,
                                         _c_void_p]),
+    "qlora_linear_fwd_grouped": (ctypes.c_int, [_c_void_p, _i64, _i64, _i32, ctypes.POINTER(_i64), _i32,
+                                                _c_void_p, _c_void_p, _c_void_p, _c_void_p, _f32, _c_void_p,
+                                                _c_void_p, _c_void_p, _sz, _c_void_p]),
+    "qlora_linear_bwd_grouped": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _i32, ctypes.POINTER(_i64),
+                                                _i32, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _f32,
+                                                _c_void_p, _c_void_p, _c_void_p, _c_void_p, _c_void_p, _sz,
+                                                _c_void_p]),
 }
 
 _lib = None
@@ -315,6 +322,62 @@ def qlora_linear_bwd(X: torch.Tensor, dY: torch.Tensor, packed: torch.Tensor,
         _dev(XA, "XA", torch.float32), dx_ptr, _dev(dA, "dA", torch.float32),
         _dev(dB, "dB", torch.float32), _dev(workspace, "workspace", torch.uint8),
         workspace.numel(), _stream(X)))
+    return dX, dA, dB
+
+
+def _group_array(group_d_out):
+    arr = (_i64 * len(group_d_out))(*[int(n) for n in group_d_out])
+    return arr, sum(int(n) for n in group_d_out)
+
+
+def qlora_linear_fwd_grouped(X: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor, A: torch.Tensor,
+                             B: torch.Tensor, s: float, group_d_out, group_rank: int, *,
+                             Y: torch.Tensor | None = None, XA: torch.Tensor | None = None,
+                             workspace: torch.Tensor | None = None):
+    """Stacked projections with block-diagonal low-rank blocks (group g: output
+    features of group_d_out[g], rank columns [g*group_rank, (g+1)*group_rank)).
+    Returns (Y bf16 [M, d_out], XA fp32 [M, r])."""
+    lib = load_library()
+    M, d_in = X.shape
+    groups, d_out = _group_array(group_d_out)
+    r = len(group_d_out) * int(group_rank)
+    if A.shape != (d_in, r) or B.shape != (r, d_out):
+        raise ValueError(f"A must be [{d_in}, {r}] and B [{r}, {d_out}]")
+    if Y is None:
+        Y = torch.empty(M, d_out, dtype=torch.bfloat16, device=X.device)
+    if XA is None:
+        XA = torch.empty(M, r, dtype=torch.float32, device=X.device)
+    workspace, _ = _workspace(M, d_in, d_out, r, X.device, workspace)
+    _check("qlora_linear_fwd_grouped", lib.qlora_linear_fwd_grouped(
+        _dev(X, "X", torch.bfloat16), M, d_in, len(group_d_out), groups, int(group_rank),
+        _dev(packed, "packed", torch.uint8), _dev(absmax, "absmax", torch.float32), _dev(A, "A", torch.bfloat16),
+        _dev(B, "B", torch.bfloat16), float(s), _dev(Y, "Y", torch.bfloat16), _dev(XA, "XA", torch.float32),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(X)))
+    return Y, XA
+
+
+def qlora_linear_bwd_grouped(X: torch.Tensor, dY: torch.Tensor, packed: torch.Tensor, absmax: torch.Tensor,
+                             A: torch.Tensor, B: torch.Tensor, s: float, XA: torch.Tensor, group_d_out,
+                             group_rank: int, *, need_dX: bool = True, workspace: torch.Tensor | None = None):
+    """Backward of qlora_linear_fwd_grouped.  Returns (dX or None, dA [d_in, r],
+    dB [r, d_out]); dB holds the diagonal blocks (zeros elsewhere)."""
+    lib = load_library()
+    M, d_in = X.shape
+    groups, d_out = _group_array(group_d_out)
+    r = len(group_d_out) * int(group_rank)
+    if dY.shape != (M, d_out):
+        raise ValueError(f"dY must be [{M}, {d_out}], got {tuple(dY.shape)}")
+    dX = torch.empty(M, d_in, dtype=torch.bfloat16, device=X.device) if need_dX else None
+    dA = torch.empty(d_in, r, dtype=torch.float32, device=X.device)
+    dB = torch.zeros(r, d_out, dtype=torch.float32, device=X.device)
+    workspace, _ = _workspace(M, d_in, d_out, r, X.device, workspace)
+    dx_ptr = _dev(dX, "dX", torch.bfloat16) if dX is not None else None
+    _check("qlora_linear_bwd_grouped", lib.qlora_linear_bwd_grouped(
+        _dev(X, "X", torch.bfloat16), _dev(dY, "dY", torch.bfloat16), M, d_in, len(group_d_out), groups,
+        int(group_rank), _dev(packed, "packed", torch.uint8), _dev(absmax, "absmax", torch.float32),
+        _dev(A, "A", torch.bfloat16), _dev(B, "B", torch.bfloat16), float(s), _dev(XA, "XA", torch.float32),
+        dx_ptr, _dev(dA, "dA", torch.float32), _dev(dB, "dB", torch.float32),
+        _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(X)))
     return dX, dA, dB
 
 

@@ -61,7 +61,8 @@ def test_workspace_bytes(lib):
     assert qlora.qlora_workspace_bytes(64, 100, 256, 8) == 0      # d_in % 64
     assert qlora.qlora_workspace_bytes(64, 256, 252, 8) == 0      # d_out % 8
     assert qlora.qlora_workspace_bytes(64, 256, 256, 0) == 0
-    assert qlora.qlora_workspace_bytes(64, 256, 256, 129) == 0
+    assert qlora.qlora_workspace_bytes(64, 256, 256, 257) == 0
+    assert qlora.qlora_workspace_bytes(64, 256, 256, 256) > 0
 
 
 FAKE = 0x10000      # 16-byte aligned, never dereferenced: validation fails first
@@ -76,7 +77,7 @@ def _fwd(lib, X=FAKE, M=64, K=256, N=256, P=FAKE, S=FAKE, A=FAKE, B=FAKE, r=8, Y
 def test_forward_argument_validation(lib):
     assert _fwd(lib, K=100) == 4
     assert _fwd(lib, N=260 - 2) == 4
-    assert _fwd(lib, r=0) == 4 and _fwd(lib, r=129) == 4
+    assert _fwd(lib, r=0) == 4 and _fwd(lib, r=257) == 4
     assert _fwd(lib, M=-1) == 2 and _fwd(lib, K=0) == 2
     assert _fwd(lib, X=None) == 1 and _fwd(lib, P=None) == 1 and _fwd(lib, XA=None) == 1
     assert _fwd(lib, X=MISALIGNED) == 3 and _fwd(lib, Y=MISALIGNED) == 3

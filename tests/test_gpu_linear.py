@@ -36,6 +36,10 @@ SMALL = [
     (96, 192, 200, 65, 1.25),      # r padded to 128
     (128, 256, 256, 128, 0.125),
     (520, 640, 520, 1, 3.0),
+    (160, 256, 320, 129, 0.5),     # r padded to 256, A padded (r % 8 != 0)
+    (200, 384, 264, 192, 0.25),    # r padded to 256: four low-rank stages
+    (64, 256, 256, 256, 0.125),    # the largest rank
+    (9, 512, 136, 200, 0.5),       # few tokens, rank above 128: the main kernel
 ]
 
 
@@ -45,7 +49,8 @@ def test_small_cases_full(case):
     check_layer(_inputs(M, K, N, r, seed=M + K), s)
 
 
-@pytest.mark.parametrize("case", [(64, 256, 256, 8, 2.0), (200, 320, 136, 24, 1.5), (257, 384, 264, 100, 0.75)],
+@pytest.mark.parametrize("case", [(64, 256, 256, 8, 2.0), (200, 320, 136, 24, 1.5), (257, 384, 264, 100, 0.75),
+                                  (130, 256, 200, 192, 0.5)],
                          ids=lambda c: "M{}_K{}_N{}_r{}".format(*c[:4]))
 def test_lora_term_dominant(case):
     """Zero base weight and B ~ N(0, 1): Y and dX are the low-rank terms alone."""

@@ -18,12 +18,16 @@ from rank_adapter_linear_nf4_b300 import synthetic
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # (d_out, d_in, r, s)
-    (256, 256, 8, 2.0),
+    # (d_out, d_in, r, s).  r % 8 == 0 takes the persistent kernel (A^T, B^T by TMA,
+    # a run of tiles per CTA); other ranks the one-tile-per-CTA kernel.
+    (256, 256, 8, 2.0),        # fewer tiles than SMs
     (136, 320, 12, 1.5),       # ragged tiles in both directions, r % 8 != 0
+    (136, 320, 16, 1.5),       # the same raggedness on the persistent kernel
+    (1000, 1280, 24, 0.5),     # last row block 104 rows, rank 24 (B^T rows past r are zero)
     (384, 512, 128, 0.125),
     (1024, 4096, 64, 0.25),
-    (4096, 4096, 16, 1.0),     # the q_proj weight
+    (4096, 4096, 16, 1.0),     # the q_proj weight: runs of ~7 tiles crossing row blocks
+    (8200, 4096, 64, 0.25),    # 65 row blocks, the last 8 rows
 ]
 
 

@@ -26,7 +26,7 @@ def _inputs(M, K, N, r, seed=0, b_std=0.01):
 
 
 CASES = [
-    # (M, d_in, d_out, r, s); an item is 32 weight rows x one 64-element block
+    # (M, d_in, d_out, r, s); an item is 16 weight rows x 256 input features
     (1, 256, 256, 16, 1.0),         # 16 units of one item
     (3, 256, 64, 8, 2.0),           # a single CTA
     (8, 4096, 64, 16, 1.0),         # four slices per row group
