@@ -28,9 +28,10 @@ What it computes, with the passage each step follows:
   weights).  The concrete format is the plainest reading: the 16-level NF4 code
   table published with QLoRA (Dettmers et al., 2023, "QLoRA: Efficient
   Finetuning of Quantized LLMs", Appendix E), blocks of 64 consecutive elements
-  of the row-major weight, one fp32 absmax per block, no second-level
-  quantisation of the absmax, two codes per byte with the first element in the
-  high nibble.
+  of the row-major weight, one fp32 absmax per block, two codes per byte with
+  the first element in the high nibble.  Optionally (row f4) the absmax itself
+  is stored in 8 bits per block with one fp32 scale per 256 blocks
+  (``quantize_absmax_dq``); the NF4 dequantisation then uses the stored value.
 
 Precision: the NF4 code decision is taken in fp32 (correctly rounded division
 w / absmax, then an exact comparison against the midpoints between adjacent
@@ -162,6 +163,51 @@ def dequantize_nf4(packed, absmax, n_out: int, n_in: int) -> np.ndarray:
     scale = np.repeat(a, BLOCK)
     prod = (NF4_CODE[q] * scale).astype(np.float32)      # one fp32 multiply
     return bf16_round(prod).reshape(n_out, n_in)
+
+
+# ---------------------------------------------------------------- row f4: the absmax stored in 8 bits
+
+DQ_GROUP = 256      # block absmax values per second-level group
+
+
+def quantize_absmax_dq(absmax) -> tuple[np.ndarray, np.ndarray]:
+    """Second-level ("double") quantisation of the block absmax (row f4).
+
+    The pages name NF4 only (page "UnSloth加速原理：CUDA内核融合与内存优化", section
+    "内核融合", ``load_in_4bit``); QLoRA (Dettmers et al., 2023, section 3,
+    "Double Quantization") stores the fp32 block constants themselves in 8 bits,
+    in groups of 256.  The plainest well-defined version is taken: per group g of
+    256 consecutive absmax values (the last group may be shorter), with c_g the
+    largest of them,
+        scale2_g = fl32(c_g / 255)           (0 when c_g == 0)
+        q8_i     = the integer nearest fl32(a_i / scale2_g), ties to even,
+                   limited to [0, 255]       (0 when scale2_g == 0)
+    so each block's scale costs one byte plus a 256th of an fp32.
+    Returns (q8 uint8 [n], scale2 float32 [ceil(n / 256)]).
+    """
+    a = np.asarray(absmax, dtype=np.float32).reshape(-1)
+    n = a.size
+    n_groups = -(-n // DQ_GROUP)
+    scale2 = np.zeros(n_groups, dtype=np.float32)
+    q8 = np.zeros(n, dtype=np.uint8)
+    for g in range(n_groups):
+        seg = a[g * DQ_GROUP:(g + 1) * DQ_GROUP]
+        c = np.float32(seg.max())
+        if c == 0.0:
+            continue
+        sc = np.float32(c / np.float32(255.0))                 # IEEE fp32 division
+        scale2[g] = sc
+        x = (seg / sc).astype(np.float32)                      # IEEE fp32 division
+        q8[g * DQ_GROUP:(g + 1) * DQ_GROUP] = np.clip(np.rint(x), 0, 255).astype(np.uint8)
+    return q8, scale2
+
+
+def dequantize_absmax_dq(q8, scale2) -> np.ndarray:
+    """The stored absmax: a'_i = fl32(q8_i * scale2_g), the block scale the NF4
+    dequantisation then uses in place of the fp32 absmax."""
+    q = np.asarray(q8, dtype=np.uint8).reshape(-1)
+    sc = np.repeat(np.asarray(scale2, dtype=np.float32), DQ_GROUP)[:q.size]
+    return (q.astype(np.float32) * sc).astype(np.float32)
 
 
 def _f64(x):

@@ -430,3 +430,52 @@ def test_swiglu_mlp_block_forward_one_hot():
     want = np.zeros((1, dm))
     want[0, 7] = 2.0 * 0.5 * expit(0.5) * -0.25
     np.testing.assert_allclose(Y, want, rtol=1e-14, atol=1e-300)
+
+
+# ---------------------------------------------------------------- row f4: 8-bit absmax
+
+def test_absmax_dq_exact_on_representable_scales():
+    """A group whose largest absmax is 255 * 2^e has scale2 = 2^e exactly, so
+    every k * 2^e (k in 0..255) is stored as k and comes back exactly."""
+    g = np.random.default_rng(21)
+    for e in (-20, -3, 0, 7):
+        k = g.integers(0, 256, size=256)
+        k[17] = 255
+        a = (k.astype(np.float64) * 2.0 ** e).astype(np.float32)
+        q, sc = O.quantize_absmax_dq(a)
+        assert sc[0] == np.float32(2.0 ** e)
+        assert np.array_equal(q.astype(np.int64), k)
+        assert np.array_equal(O.dequantize_absmax_dq(q, sc), a)
+
+
+def test_absmax_dq_brute_force_nearest_code():
+    """Each stored byte is the code whose value k * scale2 is nearest a_i among all
+    256 (searched exhaustively in fp64; a tie between two codes goes to the even
+    one), over a ragged last group, and the largest absmax of a group is 255."""
+    g = np.random.default_rng(22)
+    a = (np.abs(g.normal(size=700)) * np.exp(g.uniform(-4, 4, size=700))).astype(np.float32)
+    q, sc = O.quantize_absmax_dq(a)
+    assert sc.size == 3 and q.size == 700
+    for i in range(a.size):
+        s_g = np.float64(sc[i // 256])
+        x = np.float64(np.float32(np.float32(a[i]) / np.float32(s_g)))   # the quotient in fp32
+        d = np.abs(x - np.arange(256, dtype=np.float64))
+        best = np.flatnonzero(d == d.min())
+        want = best[0] if best.size == 1 else best[best % 2 == 0][0]
+        assert q[i] == want, i
+    for grp in range(3):
+        seg = a[grp * 256:(grp + 1) * 256]
+        assert q[grp * 256 + int(np.argmax(seg))] == 255
+
+
+def test_absmax_dq_error_bound_and_zero_groups():
+    """|a' - a| is at most half a step of the group's scale (plus fp32 rounding),
+    and an all-zero group stores zeros with scale 0."""
+    g = np.random.default_rng(23)
+    a = np.abs(g.normal(size=1024)).astype(np.float32)
+    a[256:512] = 0.0
+    q, sc = O.quantize_absmax_dq(a)
+    r = O.dequantize_absmax_dq(q, sc)
+    assert sc[1] == 0.0 and not np.any(q[256:512]) and not np.any(r[256:512])
+    step = np.repeat(sc.astype(np.float64), 256)
+    assert np.all(np.abs(r.astype(np.float64) - a) <= 0.5 * step * (1 + 2.0 ** -20) + 2.0 ** -24 * a)
