@@ -138,6 +138,30 @@ qlora_status qlora_dequant_nf4(const uint8_t* packed, const float* absmax,
                                qlora_stream_t stream);
 
 /*
+ * The block absmax stored in 8 bits (row f4, "double quantisation"; QLoRA,
+ * Dettmers et al. 2023, section 3, which the pages' load_in_4bit stands on:
+ * "UnSloth加速原理：CUDA内核融合与内存优化", section 内核融合).  Groups of 256
+ * consecutive block absmax values (the last may be shorter); per group g, with
+ * c_g its largest value,
+ *   scale2[g] = fl32(c_g / 255)  (0 when c_g == 0),
+ *   q8[i]     = the integer nearest fl32(absmax[i] / scale2[g]), ties to even,
+ *               at most 255 (0 when scale2[g] == 0),
+ * and back: absmax'[i] = fl32(q8[i] * scale2[g]).  Storage per weight element:
+ * 0.5 + 1/64 + 1/4096 bytes instead of 0.5 + 1/16.  The layer calls take the
+ * fp32 absmax': expand it (qlora_dequant_absmax_dq, n_blocks * 4 bytes of
+ * scratch) before a call; everything downstream (the NF4 dequantisation, the
+ * fused kernels) is unchanged.
+ *   absmax  [n_blocks] fp32 (read by _quantize, written by _dequant);
+ *   q8      [n_blocks] bytes; scale2 [ceil(n_blocks / 256)] fp32.
+ * Requires n_blocks >= 1; all pointers 16-byte aligned.  Asynchronous on `stream`.
+ */
+qlora_status qlora_quantize_absmax_dq(const float* absmax, int64_t n_blocks, uint8_t* q8, float* scale2,
+                                      qlora_stream_t stream);
+qlora_status qlora_dequant_absmax_dq(const uint8_t* q8, const float* scale2, int64_t n_blocks, float* absmax,
+                                     qlora_stream_t stream);
+
+
+/*
  * Merged 16-bit weight: the adapter folded into the base weight,
  *   W_out[n, k] = bf16_rne(fma(s, (A . B)[k, n], W_deq[n, k]))
  * with W_deq the qlora_dequant_nf4 expansion (bit for bit) and (A . B) the

@@ -24,6 +24,7 @@ enum KernelKind : int {
   kKindSwigluFwd,
   kKindSwigluBwd,
   kKindStreamFinish,
+  kKindAbsmaxDq,
   kNumKernelKinds
 };
 
@@ -51,6 +52,13 @@ bool take_debug_stall();
 // NF4 codec (nf4_codec.cu).
 cudaError_t launch_quantize_nf4(const uint16_t* W, int64_t n_elems, uint8_t* packed, float* absmax,
                                 cudaStream_t stream);
+// The block absmax in 8 bits (groups of kDqGroup blocks, one fp32 scale each)
+// and back.
+constexpr int kDqGroup = 256;
+cudaError_t launch_quantize_absmax_dq(const float* absmax, int64_t n, uint8_t* q8, float* scale2,
+                                      cudaStream_t stream);
+cudaError_t launch_dequant_absmax_dq(const uint8_t* q8, const float* scale2, int64_t n, float* absmax,
+                                     cudaStream_t stream);
 cudaError_t launch_dequant_nf4(const uint8_t* packed, const float* absmax, int64_t n_elems,
                                uint16_t* W_out, cudaStream_t stream);
 void nf4_levels_host(float out[16]);

@@ -221,7 +221,65 @@ __global__ void __launch_bounds__(kDeqThreads) nf4_dequant_kernel(const uint4* _
   }
 }
 
+// ---------------------------------------------------------------- the absmax in 8 bits
+
+// One warp per group of kDqGroup block absmax values: the group's largest c
+// (a shuffle max), scale2 = fl32(c / 255), and per value the nearest integer to
+// fl32(a / scale2), ties to even, limited to 255 (all zero when c == 0).
+__global__ void __launch_bounds__(256) absmax_dq_quantize_kernel(const float* __restrict__ absmax, int64_t n,
+                                                               uint8_t* __restrict__ q8, float* __restrict__ scale2) {
+  const int64_t group = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t base = group * kDqGroup;
+  if (base >= n) return;   // whole warps leave together
+  float v[kDqGroup / 32];
+  float c = 0.0f;
+#pragma unroll
+  for (int j = 0; j < kDqGroup / 32; ++j) {
+    const int64_t i = base + lane + 32 * j;
+    v[j] = i < n ? ldg_nc_f32(absmax + i) : 0.0f;
+    c = fmaxf(c, v[j]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) c = fmaxf(c, __shfl_xor_sync(0xffffffffu, c, o));
+  const float sc = c > 0.0f ? __fdiv_rn(c, 255.0f) : 0.0f;
+#pragma unroll
+  for (int j = 0; j < kDqGroup / 32; ++j) {
+    const int64_t i = base + lane + 32 * j;
+    if (i < n) q8[i] = sc > 0.0f ? static_cast<uint8_t>(min(255u, __float2uint_rn(__fdiv_rn(v[j], sc)))) : 0;
+  }
+  if (lane == 0) scale2[group] = sc;
+}
+
+// a'_i = fl32(q8_i * scale2_g).
+__global__ void __launch_bounds__(256) absmax_dq_dequant_kernel(const uint8_t* __restrict__ q8,
+                                                              const float* __restrict__ scale2, int64_t n,
+                                                              float* __restrict__ absmax) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    absmax[i] = __fmul_rn(static_cast<float>(q8[i]), ldg_nc_f32(scale2 + i / kDqGroup));
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_absmax_dq(const float* absmax, int64_t n, uint8_t* q8, float* scale2,
+                                      cudaStream_t stream) {
+  const int64_t groups = (n + kDqGroup - 1) / kDqGroup;
+  const int64_t grid = (groups + 7) / 8;   // 8 warps per CTA
+  LaunchScope scope(kKindAbsmaxDq, stream);
+  absmax_dq_quantize_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(absmax, n, q8, scale2);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_absmax_dq(const uint8_t* q8, const float* scale2, int64_t n, float* absmax,
+                                     cudaStream_t stream) {
+  const int64_t grid = std::min<int64_t>((n + 255) / 256, 148 * 8);
+  LaunchScope scope(kKindAbsmaxDq, stream);
+  absmax_dq_dequant_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(q8, scale2, n, absmax);
+  return cudaGetLastError();
+}
+
+
 
 void nf4_levels_host(float out[16]) {
   for (int i = 0; i < 16; ++i) out[i] = kNF4LevelsHost[i];

@@ -96,7 +96,7 @@ std::vector<cudaEvent_t> g_free_events;
 const char* const kKindNames[qlora::kNumKernelKinds] = {
     "nf4_quantize", "nf4_dequant", "lora_pad_A", "lora_rows_T", "lora_rows_G",
     "lora_red_dA_dB", "lora_main_fwd", "lora_main_dX", "lora_merge", "lora_stream_fwd", "swiglu_fwd", "swiglu_bwd",
-    "lora_stream_finish"};
+    "lora_stream_finish", "nf4_absmax_dq"};
 
 cudaEvent_t take_event() {
   if (!g_free_events.empty()) {
@@ -256,6 +256,24 @@ qlora_status qlora_dequant_nf4(const uint8_t* packed, const float* absmax, int64
   if (!aligned16(packed) || !aligned16(absmax) || !aligned16(W_out)) return QLORA_ERR_ALIGN;
   cudaError_t e = qlora::launch_dequant_nf4(packed, absmax, n_out * n_in, W_out,
                                             reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+qlora_status qlora_quantize_absmax_dq(const float* absmax, int64_t n_blocks, uint8_t* q8, float* scale2,
+                                      qlora_stream_t stream) {
+  if (n_blocks < 1 || n_blocks > kMaxDim * 8) return QLORA_ERR_SHAPE;
+  if (!absmax || !q8 || !scale2) return QLORA_ERR_NULL;
+  if (!aligned16(absmax) || !aligned16(q8) || !aligned16(scale2)) return QLORA_ERR_ALIGN;
+  cudaError_t e = qlora::launch_quantize_absmax_dq(absmax, n_blocks, q8, scale2, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
+}
+
+qlora_status qlora_dequant_absmax_dq(const uint8_t* q8, const float* scale2, int64_t n_blocks, float* absmax,
+                                     qlora_stream_t stream) {
+  if (n_blocks < 1 || n_blocks > kMaxDim * 8) return QLORA_ERR_SHAPE;
+  if (!absmax || !q8 || !scale2) return QLORA_ERR_NULL;
+  if (!aligned16(absmax) || !aligned16(q8) || !aligned16(scale2)) return QLORA_ERR_ALIGN;
+  cudaError_t e = qlora::launch_dequant_absmax_dq(q8, scale2, n_blocks, absmax, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QLORA_OK : cuda_fail(e);
 }
 

@@ -38,6 +38,8 @@ _SIGNATURES = {
     "qlora_quantize_nf4": (ctypes.c_int, [_c_void_p, _i64, _i64, _c_void_p, _c_void_p, _c_void_p]),
     "qlora_dequant_nf4": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _i64, _c_void_p, _c_void_p]),
     "qlora_workspace_bytes": (_sz, [_i64, _i64, _i64, _i32]),
+    "qlora_quantize_absmax_dq": (ctypes.c_int, [_c_void_p, _i64, _c_void_p, _c_void_p, _c_void_p]),
+    "qlora_dequant_absmax_dq": (ctypes.c_int, [_c_void_p, _c_void_p, _i64, _c_void_p, _c_void_p]),
     "qlora_linear_fwd": (ctypes.c_int, [_c_void_p, _i64, _i64, _i64, _c_void_p, _c_void_p,
                                         _c_void_p, _c_void_p, _i32, _f32, _c_void_p, _c_void_p,
                                         _c_void_p, _sz, _c_void_p]),
@@ -241,6 +243,30 @@ def qlora_swiglu_bwd(gu: torch.Tensor, dh: torch.Tensor, out: torch.Tensor | Non
         _dev(gu, "gu", torch.bfloat16), _dev(dh, "dh", torch.bfloat16), M, d_ff,
         _dev(out, "dgu", torch.bfloat16), _stream(gu)))
     return out
+
+
+def qlora_quantize_absmax_dq(absmax: torch.Tensor):
+    """The block absmax in 8 bits: (q8 uint8 [n], scale2 fp32 [ceil(n / 256)])."""
+    lib = load_library()
+    n = absmax.numel()
+    q8 = torch.empty(n, dtype=torch.uint8, device=absmax.device)
+    scale2 = torch.empty(-(-n // 256), dtype=torch.float32, device=absmax.device)
+    _check("qlora_quantize_absmax_dq", lib.qlora_quantize_absmax_dq(
+        _dev(absmax, "absmax", torch.float32), n, _dev(q8, "q8", torch.uint8), _dev(scale2, "scale2", torch.float32),
+        _stream(absmax)))
+    return q8, scale2
+
+
+def qlora_dequant_absmax_dq(q8: torch.Tensor, scale2: torch.Tensor, *, absmax: torch.Tensor | None = None):
+    """The fp32 block absmax the layer calls take, from its 8-bit storage."""
+    lib = load_library()
+    n = q8.numel()
+    if absmax is None:
+        absmax = torch.empty(n, dtype=torch.float32, device=q8.device)
+    _check("qlora_dequant_absmax_dq", lib.qlora_dequant_absmax_dq(
+        _dev(q8, "q8", torch.uint8), _dev(scale2, "scale2", torch.float32), n, _dev(absmax, "absmax", torch.float32),
+        _stream(q8)))
+    return absmax
 
 
 def _workspace(M, d_in, d_out, r, device, workspace):

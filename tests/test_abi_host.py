@@ -137,3 +137,28 @@ def test_stall_hook_is_off_by_default_and_rejects_negative(lib):
     from rank_adapter_linear_nf4_b300 import qlora
     assert lib.qlora_debug_stall_main_launches(-1) == 2     # QLORA_ERR_SHAPE, nothing armed
     assert lib.qlora_debug_stall_main_launches(0) == 0
+
+
+def test_absmax_dq_argument_validation(lib):
+    assert lib.qlora_quantize_absmax_dq(FAKE, 0, FAKE, FAKE, None) == 2
+    assert lib.qlora_quantize_absmax_dq(None, 8, FAKE, FAKE, None) == 1
+    assert lib.qlora_quantize_absmax_dq(FAKE, 8, MISALIGNED, FAKE, None) == 3
+    assert lib.qlora_dequant_absmax_dq(FAKE, FAKE, -1, FAKE, None) == 2
+    assert lib.qlora_dequant_absmax_dq(FAKE, None, 8, FAKE, None) == 1
+    assert lib.qlora_dequant_absmax_dq(FAKE, FAKE, 8, MISALIGNED, None) == 3
+
+
+def test_grouped_argument_validation(lib):
+    import ctypes
+    groups = (ctypes.c_int64 * 3)(256, 128, 128)
+
+    def fwd(n=3, g=groups, width=64, M=16, K=256):
+        return lib.qlora_linear_fwd_grouped(FAKE, M, K, n, g, width, FAKE, FAKE, FAKE, FAKE, 1.0, FAKE, FAKE,
+                                            FAKE, 1 << 30, None)
+    assert fwd(g=None) == 1
+    assert fwd(n=0) == 4 and fwd(n=9) == 4
+    assert fwd(width=32) == 4                                # a multiple of 64
+    assert fwd(width=128) == 4                               # 3 x 128 > 256
+    assert fwd(g=(ctypes.c_int64 * 3)(200, 128, 128)) == 4   # a group but the last not a multiple of 128
+    assert fwd(g=(ctypes.c_int64 * 3)(256, 0, 128)) == 2
+    assert fwd(K=100) == 4
