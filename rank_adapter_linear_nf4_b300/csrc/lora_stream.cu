@@ -163,19 +163,6 @@ __device__ __forceinline__ uint32_t lut_pair(uint32_t lut_lane, uint32_t w, uint
   return lds32(prmt(w, lut_lane, sel));
 }
 
-// 16 bytes of shared memory if `on`, else zeros.
-__device__ __forceinline__ uint4 ld_shared_v4_if(uint32_t addr, bool on) {
-  uint4 v;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.u32 p, %5, 0;\n\t"
-      "mov.u32 %0, 0;\n\tmov.u32 %1, 0;\n\tmov.u32 %2, 0;\n\tmov.u32 %3, 0;\n\t"
-      "@p ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}"
-      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-      : "r"(addr), "r"(static_cast<uint32_t>(on)));
-  return v;
-}
-
 // Blocks of slice s.
 __device__ __forceinline__ int slice_blocks(const StreamParams& p, int s) {
   return min(kSliceBlocks, p.kb - s * kSliceBlocks);
@@ -193,10 +180,12 @@ struct SliceSplit {
 };
 
 // One item's MMAs: acc += absmax * (codes of 16 rows x 4 blocks) . X.  Token
-// rows at or past M are not read (their MMA columns are never stored).
+// rows at or past M are not read: their lanes' X fragments stay zero (and
+// their MMA columns are never stored).
 template <int MT>
-__device__ __forceinline__ void compute_item(uint32_t code_slot, uint32_t abs_slot, uint32_t x_row0, int blk0,
-                                             uint32_t lut_lane, int g4, int t, int M, float (&acc)[MT][4]) {
+__device__ __forceinline__ void compute_item(uint32_t code_slot, uint32_t abs_slot, const uint8_t* x_row0, int blk0,
+                                             uint32_t lut_lane, int g4, int t, const bool (&live)[MT],
+                                             uint4 (&x)[MT][2], float (&acc)[MT][4]) {
   const uint32_t ra = static_cast<uint32_t>(g4), rb = static_cast<uint32_t>(g4 + 8);
   const uint4 am_a4 = ld_shared_v4(abs_slot + ra * 16u);   // the item's four block scales, rows g and g+8
   const uint4 am_b4 = ld_shared_v4(abs_slot + rb * 16u);
@@ -210,14 +199,14 @@ __device__ __forceinline__ void compute_item(uint32_t code_slot, uint32_t abs_sl
     const uint2 cb = lds64(ca_addr + 1024u);
     const float am_a = __uint_as_float(blk == 0 ? am_a4.x : blk == 1 ? am_a4.y : blk == 2 ? am_a4.z : am_a4.w);
     const float am_b = __uint_as_float(blk == 0 ? am_b4.x : blk == 1 ? am_b4.y : blk == 2 ? am_b4.z : am_b4.w);
-    uint4 x[MT][2];
 #pragma unroll
     for (int j = 0; j < MT; ++j) {
-      const uint32_t src = x_row0 + static_cast<uint32_t>(j * 8 * kXPitch) +
-                           static_cast<uint32_t>(((blk0 + blk) * 64 + 16 * t) * 2);
-      const bool live = 8 * j + g4 < M;
-      x[j][0] = ld_shared_v4_if(src, live);
-      x[j][1] = ld_shared_v4_if(src + 16, live);
+      // a lane of an absent token keeps the zeros its fragment started with
+      const uint4* src = reinterpret_cast<const uint4*>(x_row0 + j * 8 * kXPitch + ((blk0 + blk) * 64 + 16 * t) * 2);
+      if (live[j]) {
+        x[j][0] = src[0];
+        x[j][1] = src[1];
+      }
     }
     float d[MT][4];
 #pragma unroll
@@ -412,7 +401,14 @@ __global__ void __launch_bounds__(StreamCfg<MT>::kThreads, 1)
   // every lane acquires the bulk-copied X itself
   bool ok = mbar_wait(x_bar, 0, ab);
   const uint32_t lut_lane = lay.lut | (static_cast<uint32_t>(lane) << 2);
-  const uint32_t x_row0 = lay.x + static_cast<uint32_t>(g4 * kXPitch);
+  const uint8_t* const x_row0 = smem_raw + (lay.x - window) + g4 * kXPitch;
+  bool live[MT];
+  uint4 xfrag[MT][2];
+#pragma unroll
+  for (int j = 0; j < MT; ++j) {
+    live[j] = 8 * j + g4 < p.M;
+    xfrag[j][0] = xfrag[j][1] = make_uint4(0u, 0u, 0u, 0u);
+  }
   float acc[MT][4];
 #pragma unroll
   for (int j = 0; j < MT; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
@@ -426,7 +422,7 @@ __global__ void __launch_bounds__(StreamCfg<MT>::kThreads, 1)
       break;
     }
     compute_item<MT>(code_ring + slot * kCodeSlot, abs_ring + slot * kAbsSlot, x_row0, cit * kItemBlocks, lut_lane,
-                     g4, t, p.M, acc);
+                     g4, t, live, xfrag, acc);
     // the slot's codes have been read by every lane: refill it kDepth items ahead
     __syncwarp();
     if (lane == 0 && k + kDepth < n_items) {
