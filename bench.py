@@ -75,12 +75,22 @@ def step_bytes(sh) -> float:
     return fwd + bwd
 
 
-def sources_hash() -> str:
-    """Hash of the CUDA sources: a stored ncu traffic figure counts only for these."""
+# The source files each measured kernel is built from (a stored traffic figure
+# counts only while they are unchanged).
+KERNEL_SOURCES = {
+    "lora_main_fwd": ("lora_kernels.cu", "nf4_lut.cuh", "ptx.cuh", "kernels.h"),
+    "lora_main_dX": ("lora_kernels.cu", "nf4_lut.cuh", "ptx.cuh", "kernels.h"),
+    "lora_stream_fwd": ("lora_stream.cu", "nf4_lut.cuh", "ptx.cuh", "kernels.h"),
+}
+
+
+def sources_hash(kernel: str) -> str:
+    """Hash of the CUDA sources `kernel` is built from."""
     import hashlib
     h = hashlib.sha1()
     csrc = os.path.join(ROOT, "rank_adapter_linear_nf4_b300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    files = KERNEL_SOURCES.get(kernel) or tuple(sorted(os.listdir(csrc)))
+    for fn in files:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
@@ -95,7 +105,7 @@ def stored_traffic(kernel: str, workload: str):
     except (OSError, ValueError):
         return None
     e = t.get(f"{kernel}@{workload}")
-    if not e or e.get("sources") != sources_hash():
+    if not e or e.get("sources") != sources_hash(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
