@@ -683,9 +683,14 @@ def run_ours(args):
     codec = codec_rooflines(sh, wl.sets, dev, peaks)
 
     extra = {}
+    blocks = {}
     if not args.no_extra:
         del wl
         torch.cuda.empty_cache()
+        try:
+            blocks = measure_blocks(dev, timed, peaks)
+        except Exception as e:   # report, do not fail the run
+            blocks = {"error": f"{type(e).__name__}: {e}"[:300]}
         for name in EXTRA_CONFIGS:
             if name == sh.name:
                 continue
@@ -718,6 +723,7 @@ def run_ours(args):
         "profiled_clocks": prof_clocks,
         "gpu_launches": launches,
         "hbm_kernels": codec,
+        "blocks": blocks,
         "cuda_graph": graph,
         "clocks": clocks,
         "e2e": e2e,
@@ -793,6 +799,91 @@ def graph_timing(step, n_sets, flops, world, timed, replays=20):
         return {"error": f"{type(e).__name__}: {e}"[:200]}
     return {"ms_per_step": ms, "value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "steps_per_graph": per_graph, "replays": replays}
+
+
+def measure_blocks(dev, timed, peaks, reps=10):
+    """Rows f3 and f1 as whole calls, each beside its plain form:
+    * the SwiGLU MLP block of Llama-3-8B (8192 tokens, 4096 -> 14336 -> 4096,
+      rank 64 on gate, up and down), forward + backward, with the gate fused
+      into the layers' epilogues against the block with the separate gate kernels;
+    * q/k/v of Llama-3-8B (4096 tokens, 4096 -> 4096 + 1024 + 1024, rank 64 each)
+      as one grouped layer call against three layer calls, forward + backward.
+    Inputs are larger than L2; each form is timed over `reps` back-to-back runs."""
+    import torch
+    from rank_adapter_linear_nf4_b300 import mlp, multi, qlora, synthetic
+    out = {}
+    M, dm, dff, r = 8192, 4096, 14336, 64
+    s = 16.0 / r
+    X, dY = (t.to(dev) for t in synthetic.activations(M, dm, dm, seed=41))
+    Wg, Ag, Bg = (t.to(dev) for t in synthetic.weights(dm, dff, r, seed=42))
+    Wu, Au, Bu = (t.to(dev) for t in synthetic.weights(dm, dff, r, seed=43))
+    Wd, Ad, Bd = (t.to(dev) for t in synthetic.weights(dff, dm, r, seed=44))
+    pd, ad = qlora.qlora_quantize_nf4(Wd)
+    down = mlp.Layer(pd, ad, Ad, Bd)
+    pi, ai = qlora.qlora_quantize_nf4(mlp.interleave_weights(Wg, Wu))
+    Ai, Bi = mlp.interleave_adapters(Ag, Bg, Au, Bu)
+    gu_fused = mlp.Layer(pi, ai, Ai, Bi)
+    ps, as_ = qlora.qlora_quantize_nf4(torch.cat([Wg, Wu], dim=0).contiguous())
+    As, Bs = multi.stack_adapters([Ag, Au], [Bg, Bu])
+    gu_plain = mlp.Layer(ps, as_, As, Bs)
+    del Wg, Wu, Wd
+
+    def fused(i):
+        Y, saved = mlp.swiglu_mlp_fwd(X, gu_fused, down, s)
+        mlp.swiglu_mlp_bwd(X, dY, saved, gu_fused, down, s)
+
+    def plain(i):
+        Y, saved = mlp.swiglu_mlp_fwd_unfused(X, gu_plain, down, s)
+        mlp.swiglu_mlp_bwd_unfused(X, dY, saved, gu_plain, down, s)
+
+    flops = (step_flops(synthetic.LayerShape("gu", M, dm, 2 * dff, 2 * r, 16.0)) +
+             step_flops(synthetic.LayerShape("d", M, dff, dm, r, 16.0)))
+    res = {"workload": f"SwiGLU MLP block, {M} tokens, {dm} -> {dff} -> {dm}, rank {r} (gate/up layer 2 x {r})"}
+    for name, fn in (("fused", fused), ("separate_gate", plain)):
+        for i in range(2):
+            fn(i)
+        ms = timed(fn, reps)[0] / reps
+        res[name] = {"ms_per_step": ms, "tflops": flops / (ms * 1e-3) / 1e12}
+    res["saved_ms"] = res["separate_gate"]["ms_per_step"] - res["fused"]["ms_per_step"]
+    out["swiglu_mlp_block"] = res
+    del X, dY, down, gu_fused, gu_plain
+    torch.cuda.empty_cache()
+
+    M, K, outs, r = 4096, 4096, (4096, 1024, 1024), 64
+    s = 16.0 / r
+    X, _ = synthetic.activations(M, K, 8, seed=51)
+    X = X.to(dev)
+    layers = [tuple(t.to(dev) for t in synthetic.weights(K, n, r, seed=52 + i)) for i, n in enumerate(outs)]
+    g = torch.Generator(device=dev).manual_seed(53)
+    dY = torch.randn(M, sum(outs), device=dev, generator=g).to(torch.bfloat16)
+    Ws, As, Bs = [w for w, _, _ in layers], [a for _, a, _ in layers], [b for _, _, b in layers]
+    p = multi.packing(Ws, As)
+    A_cat, B_cat = multi.stack_adapters(As, Bs, p)
+    pk, am = qlora.qlora_quantize_nf4(multi.stack_weights(Ws))
+    sep = [(qlora.qlora_quantize_nf4(w), a, b) for w, a, b in layers]
+    dYs = [dY[:, sl].contiguous() for sl in p.out_slices()]
+
+    def grouped(i):
+        _, _, T = multi.multi_linear_fwd(X, pk, am, A_cat, B_cat, s, p)
+        multi.multi_linear_bwd(X, dY, pk, am, A_cat, B_cat, s, T, p)
+
+    def separate(i):
+        for ((pq, aq), a, b), dy in zip(sep, dYs):
+            _, T = qlora.qlora_linear_fwd(X, pq, aq, a, b, s)
+            qlora.qlora_linear_bwd(X, dy, pq, aq, a, b, s, T)
+
+    flops = sum(step_flops(synthetic.LayerShape("p", M, K, n, r, 16.0)) for n in outs)
+    res = {"workload": f"q/k/v, {M} tokens, {K} -> {' + '.join(map(str, outs))}, rank {r} each",
+           "layout": "grouped" if p.grouped else "dense"}
+    for name, fn in (("one_call", grouped), ("three_calls", separate)):
+        for i in range(2):
+            fn(i)
+        ms = timed(fn, reps)[0] / reps
+        res[name] = {"ms_per_step": ms, "tflops": flops / (ms * 1e-3) / 1e12}
+    res["note"] = "three_calls leaves the three dX to be summed; one_call returns their sum"
+    out["stacked_qkv"] = res
+    torch.cuda.empty_cache()
+    return out
 
 
 def codec_rooflines(sh, sets, dev, peaks, reps=20):

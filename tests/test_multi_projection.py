@@ -112,6 +112,7 @@ CASES = [
     (8, 1024, (1024, 256, 256), (64, 64, 64), 0.25, None),    # the same with 8 tokens
     (192, 512, (1408, 1408), (64, 64), 0.25, None),           # gate/up at rank 64: grouped
     (130, 512, (512, 256, 200), (16, 8, 24), 0.5, True),      # grouped with padded ranks, ragged last group
+    (8, 512, (1408, 1408), (64, 64), 0.25, True),             # grouped, 8 tokens: the token-stream forward
 ]
 
 
