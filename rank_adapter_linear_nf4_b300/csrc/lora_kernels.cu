@@ -398,8 +398,10 @@ __global__ void __launch_bounds__(kSkThreads, 1)
 
 constexpr int kEpiChunk = 32;        // tokens per epilogue store
 constexpr int kMinSkStages = 16;     // fewest stages a CTA takes in the split remainder
-// warp 0: TMA for the token operand; warp 1: MMA; warps 2-9: dequant; warps 10-13: epilogue;
-// warp 14: TMA for the NF4 codes and absmax (its own ring, so code latency never holds up operand loads)
+// warp 0: TMA for the token operand; warp 1: MMA (in the odd CTA of a pair: the relay of its
+// stages to the even CTA, whose thread issues the pair's MMAs); warps 2-9: dequant; warps 10-13:
+// epilogue; warp 14: TMA for the NF4 codes and absmax (its own ring, so code latency never holds
+// up operand loads)
 constexpr int kMainThreads = 480;
 
 // Ring depths, as deep as shared memory allows.  With few tokens per tile the
@@ -408,16 +410,24 @@ constexpr int kMainThreads = 480;
 constexpr int main_stages(int bn) { return bn <= 64 ? 8 : 4; }
 constexpr int raw_stages(int bn) { return (bn == 32 || bn == 128) ? 8 : 4; }
 
-template <int BN>
+// kPair: the CTA pair's UMMA (cta_group::2, M = 256) covers 256 output
+// features (128 per CTA, each CTA expanding its own W rows) and the BN tokens
+// of the tile, each CTA staging half of them.  Per SM a stage is then 32 KB
+// instead of 48 (a ring of six fits instead of four), and the tensor core
+// reads and TMA writes half the token rows: fewer shared-memory bytes per
+// flop, which also lowers the power drawn per flop.
+template <int BN, bool kPair = false>
 struct MainSmem {
-  static constexpr int kStages = main_stages(BN);
-  static constexpr int kRaw = raw_stages(BN);
+  static constexpr int kActRows = kPair ? BN / 2 : BN;   // token rows staged by this CTA
+  // a pair's 32 KB stages leave room for six in the ring (slots are g % kStages)
+  static constexpr int kStages = kPair ? 6 : main_stages(kActRows);
+  static constexpr int kRaw = kPair ? 4 : raw_stages(kActRows);
   // one UMMA of N = BN per K step (at most 256); two TMEM accumulators of BN
   // columns, so the epilogue of one piece overlaps the main loop of the next
   static constexpr int kMmaN = BN < 256 ? BN : 256;
-  static constexpr int kHalves = BN / kMmaN;
+  static constexpr int kHalves = kPair ? 1 : BN / kMmaN;
   static constexpr int kAccs = 2;
-  static constexpr int kActBytes = BN * 128;      // BN tokens x 64 contraction
+  static constexpr int kActBytes = kActRows * 128;   // staged tokens x 64 contraction
   static constexpr int kWBytes = kTileP * 128;    // 128 features x 64 contraction
   static constexpr int kStageBytes = kActBytes + kWBytes;
   static constexpr int kCodeBytes = 4096;         // Y: 128 rows x 32 B; dX: 64 rows x 64 B
@@ -427,7 +437,7 @@ struct MainSmem {
   static constexpr int kChunkBytes = kEpiChunk * kTileP * 2;   // two [32 tokens][64 features] halves
   static constexpr int kStagingOffset = kRawOffset + kRaw * kRawBytes;
   static constexpr int kBarOffset = kStagingOffset + kChunkBytes;
-  static constexpr int kBarBytes = 8 * (2 * kStages + 2 * kRaw + 5);
+  static constexpr int kBarBytes = 8 * (3 * kStages + 2 * kRaw + 5);
   static constexpr int kBytes = kBarOffset + 512 + 1024;
   static_assert(kBarBytes <= 512, "barrier area");
   static_assert(kBytes <= 232448, "shared memory budget");
@@ -518,12 +528,15 @@ __device__ __forceinline__ int sk_owner(const MainParams& p, int64_t x) {
 // Partial-tile slot of CTA c's piece of split tile j: 0 for the first tile of
 // its range, 1 for the last (a range holds at most two pieces that are not
 // whole tiles).
-template <int BN>
-__device__ __forceinline__ float* sk_slot(const MainParams& p, int c, int j) {
+// With CTA pairs the split ranges belong to pairs and each CTA of pair c
+// (rank 0 or 1) has its own two slots.
+template <int BN, bool kPair>
+__device__ __forceinline__ float* sk_slot(const MainParams& p, int c, int j, int rank) {
   const int total = p.num_kt + p.num_lt;
   const int64_t len = static_cast<int64_t>(p.sk_tiles) * total;
   const int first = static_cast<int>((len * c / p.sk_ctas) / total);
-  return p.partials + static_cast<int64_t>(2 * c + (j == first ? 0 : 1)) * (kTileP * BN);
+  const int owner = kPair ? 2 * c + rank : c;
+  return p.partials + static_cast<int64_t>(2 * owner + (j == first ? 0 : 1)) * (kTileP * BN);
 }
 
 // Walks this CTA's stages one at a time (or n at a time) across its pieces.
@@ -561,7 +574,7 @@ __device__ __forceinline__ float ld_global_cg_f32(const float* ptr) {
 // absmax values) of each stage arrive by TMA in a ring of their own; TMA
 // zero-fills rows and columns outside W, so outside W the dequantised operand
 // is zero without per-thread bounds checks.
-template <int BN, bool kTrans, bool kAbsTma>
+template <int BN, bool kTrans, bool kAbsTma, bool kPair>
 __global__ void __launch_bounds__(kMainThreads, 1)
     lora_main_kernel(const __grid_constant__ CUtensorMap map_act,    // X or dY, box {64, BN}
                      const __grid_constant__ CUtensorMap map_lact,   // bf16(s*T) or bf16(s*G), box {64, BN}
@@ -571,7 +584,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                      const __grid_constant__ CUtensorMap map_abs,    // absmax [N, K/64]; Y box {4, 128}, dX box {4, 64}
                      const __grid_constant__ CUtensorMap map_h,      // gate_fwd: h [M, N/2], box {64, 32}, 128-B swizzle
                      const MainParams p) {
-  using S = MainSmem<BN>;
+  using S = MainSmem<BN, kPair>;
   constexpr int kMainStages = S::kStages;
   constexpr int kRaw = S::kRaw;
   extern __shared__ uint8_t smem_raw[];
@@ -591,12 +604,18 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   auto tmem_full = [&](int a) { return bar0 + 8u * (2 * kMainStages + 2 * kRaw + a); };
   auto tmem_empty = [&](int a) { return bar0 + 8u * (2 * kMainStages + 2 * kRaw + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * kMainStages + 2 * kRaw + 4);
+  // pair only, in the even CTA: the odd CTA's stage i is in place too
+  auto pfull = [&](int i) { return bar0 + 8u * (2 * kMainStages + 2 * kRaw + 5 + i); };
   auto raw_slot = [&](int i) { return base + S::kRawOffset + static_cast<uint32_t>(i * S::kRawBytes); };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = p.num_kt + p.num_lt;
-  const int cta = static_cast<int>(blockIdx.x);
-  const int grid = static_cast<int>(gridDim.x);
+  // schedule units: CTAs, or CTA pairs (cluster of two; rank 0 issues the UMMAs)
+  const int rank = kPair ? static_cast<int>(cluster_ctarank()) : 0;
+  const int cta = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int grid = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  // first output feature of this CTA's rows of a tile
+  auto feat0 = [&](int tile) { return (tile % p.p_tiles) * (kPair ? 2 * kTileP : kTileP) + rank * kTileP; };
   int g_end = 0;   // stages this CTA runs
   {
     int tile, sb, se;
@@ -615,10 +634,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       mbar_init(raw_empty(i), 4);   // the 4 warps of the group that reads the slot
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(tmem_full(a), 1);   // MMA commit
-      mbar_init(tmem_empty(a), 4);  // the 4 epilogue warps
+      mbar_init(tmem_full(a), 1);                // MMA commit
+      mbar_init(tmem_empty(a), kPair ? 8 : 4);   // the epilogue warps (of both CTAs of a pair)
     }
     mbar_init(drain_bar, 1);
+    if (kPair)
+      for (int i = 0; i < kMainStages; ++i) mbar_init(pfull(i), 1);   // the odd CTA's relay
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -630,9 +651,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     tma_prefetch_map(&map_code);
     if (kAbsTma) tma_prefetch_map(&map_abs);
   }
-  if (warp == 1) tmem_alloc(smem_u32(&s_tmem), S::kAccs * BN);
+  if (warp == 1) {
+    if (kPair) tmem_alloc_pair(smem_u32(&s_tmem), S::kAccs * BN);
+    else tmem_alloc(smem_u32(&s_tmem), S::kAccs * BN);
+  }
   tc_fence_before_sync();
   __syncthreads();
+  // a pair: the peer's barriers are initialised before any arrival reaches them
+  if (kPair) cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = s_tmem;
 
@@ -646,10 +672,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       bool lora_ready = false, stop = false;
       int tile, sb, se;
       for (int idx = 0; !stop && main_piece(p, cta, grid, idx, tile, sb, se); ++idx) {
-        const int p0 = (tile % p.p_tiles) * kTileP;
-        const int t0 = (tile / p.p_tiles) * BN;
+        const int p0 = feat0(tile);
+        const int t0 = (tile / p.p_tiles) * BN + rank * S::kActRows;   // this CTA's token rows
         for (int s = sb; s < se; ++s, ++g) {
-          const int slot = g & (kMainStages - 1);
+          const int slot = g % kMainStages;
           if (!mbar_wait(empty(slot), ((g / kMainStages) & 1) ^ 1, ab)) {
             stop = true;
             break;
@@ -702,9 +728,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       bool stop = false;
       int tile, sb, se;
       for (int idx = 0; !stop && main_piece(p, cta, grid, idx, tile, sb, se); ++idx) {
-        const int p0 = (tile % p.p_tiles) * kTileP;
+        const int p0 = feat0(tile);
         for (int s = sb; s < se; ++s, ++g) {
-          const int slot = g & (kRaw - 1);
+          const int slot = g % kRaw;
           if (!mbar_wait(raw_empty(slot), ((g / kRaw) & 1) ^ 1, ab)) {
             stop = true;
             break;
@@ -729,12 +755,25 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         mbar_wait(raw_full(q % kRaw), (q / kRaw) & 1, ab, false);
     }
     __syncwarp();
+  } else if (warp == 1 && kPair && rank != 0) {
+    // ---------------- odd CTA of a pair: relays "stage in place" to the even CTA,
+    // whose thread issues the pair's UMMAs
+    if (lane == 0) {
+      const uint32_t peer_pfull0 = map_to_cta(pfull(0), 0);
+      for (int g = 0; g < g_end; ++g) {
+        const int slot = g % kMainStages;
+        if (!mbar_wait(full(slot), (g / kMainStages) & 1, ab)) break;
+        mbar_arrive_cluster(peer_pfull0 + 8u * slot);
+      }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer
     if (lane == 0) {
       // A operand majorness: Y -- W tile K-major, B tile MN-major; dX -- W tile MN-major, A tile K-major
-      constexpr uint32_t idesc_w = umma_idesc_bf16(kTileP, S::kMmaN, kTrans ? 1 : 0, 0);
-      constexpr uint32_t idesc_l = umma_idesc_bf16(kTileP, S::kMmaN, kTrans ? 0 : 1, 0);
+      constexpr int kMmaM = kPair ? 2 * kTileP : kTileP;
+      constexpr uint32_t idesc_w = umma_idesc_bf16(kMmaM, S::kMmaN, kTrans ? 1 : 0, 0);
+      constexpr uint32_t idesc_l = umma_idesc_bf16(kMmaM, S::kMmaN, kTrans ? 0 : 1, 0);
       // descriptors: fixed fields once, the start address (16-byte units) added per MMA
       const uint64_t a_hi_k = sw128_desc(0, 16, 1024), a_hi_mn = sw128_desc(0, 8192, 1024);
       const uint64_t b_hi = sw128_desc(0, 16, 1024);
@@ -752,10 +791,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           // token half h (rows h*256..) into accumulator columns h*256..
           const uint32_t b0 = bs + static_cast<uint32_t>(h * S::kMmaN * 128 / 16);
           const uint32_t d = tmem_d + static_cast<uint32_t>(h * S::kMmaN);
-          umma_bf16(d, a_hi | a0, b_hi | b0, idesc, first ? 0u : 1u);
-          umma_bf16(d, a_hi | (a0 + a_step), b_hi | (b0 + 2u), idesc, 1u);
-          umma_bf16(d, a_hi | (a0 + 2u * a_step), b_hi | (b0 + 4u), idesc, 1u);
-          umma_bf16(d, a_hi | (a0 + 3u * a_step), b_hi | (b0 + 6u), idesc, 1u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t ad = a_hi | (a0 + static_cast<uint32_t>(kk) * a_step);
+            const uint64_t bd = b_hi | (b0 + 2u * static_cast<uint32_t>(kk));
+            const uint32_t acc_in = (first && kk == 0) ? 0u : 1u;
+            if (kPair) umma_bf16_pair(d, ad, bd, idesc, acc_in);
+            else umma_bf16(d, ad, bd, idesc, acc_in);
+          }
         }
       };
       int g = 0;
@@ -764,30 +807,44 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       for (int idx = 0; ok && main_piece(p, cta, grid, idx, tile, sb, se); ++idx) {
         const int acc = idx % S::kAccs;
         const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(acc * BN);
-        if (!mbar_wait(tmem_empty(acc), ((idx / S::kAccs) & 1) ^ 1, ab)) break;
+        const uint32_t te_par = ((idx / S::kAccs) & 1) ^ 1;
+        if (!(kPair ? mbar_wait_cluster(tmem_empty(acc), te_par, ab) : mbar_wait(tmem_empty(acc), te_par, ab))) break;
         tc_fence_after_sync();
         int s = sb;
         while (s < se) {
-          const int slot = g & (kMainStages - 1);
-          if (!mbar_wait(full(slot), (g / kMainStages) & 1, ab)) {
+          const int slot = g % kMainStages;
+          const uint32_t fpar = (g / kMainStages) & 1;
+          if (!mbar_wait(full(slot), fpar, ab) || (kPair && !mbar_wait_cluster(pfull(slot), fpar, ab))) {
             ok = false;
             break;
           }
           // when the next stage of the piece is in place too, issue both at once
-          const int slot2 = (g + 1) & (kMainStages - 1);
-          const bool two = (s + 1 < se) && mbar_test_wait(full(slot2), ((g + 1) / kMainStages) & 1);
+          const int slot2 = (g + 1) % kMainStages;
+          const uint32_t fpar2 = ((g + 1) / kMainStages) & 1;
+          const bool two = (s + 1 < se) && mbar_test_wait(full(slot2), fpar2) &&
+                           (!kPair || mbar_test_wait_cluster(pfull(slot2), fpar2));
           tc_fence_after_sync();
           issue_stage(tmem_d, slot, s >= p.num_kt, s == sb);
           if (two) issue_stage(tmem_d, slot2, s + 1 >= p.num_kt, false);
-          umma_commit(empty(slot));
-          if (two) umma_commit(empty(slot2));
+          // a pair's commit frees the stage in both CTAs
+          if (kPair) {
+            umma_commit_pair(empty(slot), 3);
+            if (two) umma_commit_pair(empty(slot2), 3);
+          } else {
+            umma_commit(empty(slot));
+            if (two) umma_commit(empty(slot2));
+          }
           s += two ? 2 : 1;
           g += two ? 2 : 1;
         }
-        if (ok) umma_commit(tmem_full(acc));
+        if (ok) {
+          if (kPair) umma_commit_pair(tmem_full(acc), 3);
+          else umma_commit(tmem_full(acc));
+        }
       }
       // every MMA issued by this thread has completed once drain_bar flips
-      umma_commit(drain_bar);
+      if (kPair) umma_commit_pair(drain_bar, 1);
+      else umma_commit(drain_bar);
       mbar_wait(drain_bar, 0, ab, false);
     }
     __syncwarp();
@@ -834,15 +891,15 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     cur.advance(p, cta, grid, grp);
     nxt = cur;
     nxt.advance(p, cta, grid, 2);
-    float am_next = (grp < g_end) ? absmax_direct(cur.s, (cur.tile % p.p_tiles) * kTileP) : 0.0f;
+    float am_next = (grp < g_end) ? absmax_direct(cur.s, feat0(cur.tile)) : 0.0f;
     for (int g = grp; g < g_end; g += 2) {
       const int s = cur.s;
-      const int p0 = (cur.tile % p.p_tiles) * kTileP;
+      const int p0 = feat0(cur.tile);
       const float am_direct = am_next;
-      am_next = (g + 2 < g_end) ? absmax_direct(nxt.s, (nxt.tile % p.p_tiles) * kTileP) : 0.0f;
-      const int slot = g & (kMainStages - 1);
+      am_next = (g + 2 < g_end) ? absmax_direct(nxt.s, feat0(nxt.tile)) : 0.0f;
+      const int slot = g % kMainStages;
       const uint32_t ph = (g / kMainStages) & 1;
-      const int rslot = g & (kRaw - 1);
+      const int rslot = g % kRaw;
       // every lane acquires the TMA-written codes itself (a shuffle does not order memory)
       if (!__all_sync(0xffffffffu, mbar_wait(raw_full(rslot), (g / kRaw) & 1, ab))) break;
       uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
@@ -882,6 +939,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     // lanes pair up (shuffle) so each thread stores two adjacent features of one token.
     const int quarter = warp & 3;                 // TMEM lanes 32*quarter .. +31
     const int prow = quarter * 32 + lane;         // output feature within the tile
+    // the accumulator's columns may be overwritten: a pair's UMMA issuer (even
+    // CTA) waits for the epilogue warps of both CTAs
+    const uint32_t te_remote = kPair ? map_to_cta(tmem_empty(0), 0) : 0u;
+    auto release_acc = [&](int a) {
+      if (kPair) mbar_arrive_cluster(te_remote + 8u * static_cast<uint32_t>(a));
+      else mbar_arrive(tmem_empty(a));
+    };
     const bool leader = (warp == 10 && lane == 0);
     const uint32_t staging = base + S::kStagingOffset;
     const int f_even = prow & ~1;                 // first of the two features this lane stores
@@ -941,7 +1005,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
-      if (leader && t0 + c0 < p.M) {   // boxes wholly past the last token / feature are not stored
+      // boxes wholly past the last token / feature are not stored
+      if (leader && t0 + c0 < p.M && p0 < (kTrans ? p.K : p.N)) {
         tma_store_2d(&map_out, staging, p0, t0 + c0);
         if (p0 + 64 < (kTrans ? p.K : p.N)) tma_store_2d(&map_out, staging + 4096, p0 + 64, t0 + c0);
         tma_store_commit();
@@ -974,7 +1039,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                        make_uint4(hw[k][0], hw[k][1], hw[k][2], hw[k][3]));
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
-        if (leader && t0 + c0 < p.M) {
+        if (leader && t0 + c0 < p.M && p0 < p.N) {
           tma_store_2d(&map_h, staging, p0 >> 1, t0 + c0);
           tma_store_commit();
         }
@@ -982,11 +1047,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     };
     int tile, sb, se;
     for (int idx = 0; main_piece(p, cta, grid, idx, tile, sb, se); ++idx) {
-      const int p0 = (tile % p.p_tiles) * kTileP;
-      const int t0 = (tile / p.p_tiles) * BN;
+      const int p0 = feat0(tile);
+      const int t0 = (tile / p.p_tiles) * BN;   // all BN tokens: this CTA's TMEM rows hold them
       const int acc = idx % S::kAccs;
       const uint32_t tacc = tmem_base + static_cast<uint32_t>(acc * BN) + (static_cast<uint32_t>(quarter * 32) << 16);
-      if (!__all_sync(0xffffffffu, mbar_wait(tmem_full(acc), (idx / S::kAccs) & 1, ab))) break;
+      const uint32_t tf_par = (idx / S::kAccs) & 1;
+      if (!__all_sync(0xffffffffu, kPair ? mbar_wait_cluster(tmem_full(acc), tf_par, ab)
+                                         : mbar_wait(tmem_full(acc), tf_par, ab)))
+        break;
       tc_fence_after_sync();
       if (sb == 0 && se == total) {
         // a whole tile: straight to the output
@@ -1002,13 +1070,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         // this accumulator may be overwritten by the MMA of piece idx + 2
         tc_fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(tmem_empty(acc));
+        if (lane == 0) release_acc(acc);
         continue;
       }
       // a piece of a split tile: fp32 partial to this CTA's slot, token-major
       // ([token][feature]) so that each warp store covers 128 contiguous bytes
       const int j = tile - p.dp_tiles;
-      float* col = sk_slot<BN>(p, cta, j) + prow;
+      float* col = sk_slot<BN, kPair>(p, cta, j, rank) + prow;
       for (int c0 = 0; c0 < BN; c0 += kEpiChunk) {
         uint32_t v[32];
         tmem_ld32(tacc + c0, v);
@@ -1018,7 +1086,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       }
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tmem_empty(acc));
+      if (lane == 0) release_acc(acc);
       // publish the partial; the last piece of the tile to get here finishes it
       __threadfence();
       named_bar_sync(1, 128);
@@ -1028,20 +1096,20 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       if (leader) {
         // the counters were zeroed by the previous kernel
         griddep_wait();
-        const int before = atomicAdd(p.counters + j, 1);
+        const int before = atomicAdd(p.counters + (kPair ? 2 * j + rank : j), 1);
         s_last = (before == c_last - c_first) ? 1 : 0;
       }
       named_bar_sync(1, 128);
       if (!s_last) continue;
       __threadfence();
       // contraction order: the CTA holding the first stages comes first
-      const float* src_first = sk_slot<BN>(p, c_first, j) + prow;
+      const float* src_first = sk_slot<BN, kPair>(p, c_first, j, rank) + prow;
       for (int c0 = 0; c0 < BN; c0 += kEpiChunk) {
         float f[32];
 #pragma unroll
         for (int q = 0; q < 32; ++q) f[q] = ld_global_cg_f32(src_first + (c0 + q) * kTileP);
         for (int c = c_first + 1; c <= c_last; ++c) {
-          const float* src = sk_slot<BN>(p, c, j) + prow;
+          const float* src = sk_slot<BN, kPair>(p, c, j, rank) + prow;
 #pragma unroll
           for (int q = 0; q < 32; ++q) f[q] += ld_global_cg_f32(src + (c0 + q) * kTileP);
         }
@@ -1053,10 +1121,14 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  // a pair: the even CTA's UMMAs (which read the odd CTA's shared memory and
+  // write its TMEM) have completed and no arrival is in flight before either leaves
+  if (kPair) cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, S::kAccs * BN);
+    if (kPair) tmem_dealloc_pair(tmem_base, S::kAccs * BN);
+    else tmem_dealloc(tmem_base, S::kAccs * BN);
   }
 }
 
@@ -1190,10 +1262,12 @@ struct SplitBuffers {
 };
 
 // Whole tiles for the full waves, then the stages of the remaining tiles
-// shared evenly by the CTAs (at least kMinSkStages each), when the buffers
-// for the partial tiles are there; otherwise whole tiles only.
-int plan_schedule(int tiles, int total, int bn, const SplitBuffers& sb, MainParams& mp) {
-  const int sms = sm_count();
+// shared evenly by the units (at least kMinSkStages each), when the buffers
+// for the partial tiles are there; otherwise whole tiles only.  A unit is a
+// CTA, or a CTA pair (`per_unit` = 2 CTAs, each with its own partial tiles
+// and tile counters).  Returns the number of units to launch.
+int plan_schedule(int tiles, int total, int bn, const SplitBuffers& sb, MainParams& mp, int sms,
+                  int per_unit = 1) {
   const int full = tiles / sms, rem = tiles % sms;
   mp.sk_tiles = 0;
   mp.sk_ctas = 0;
@@ -1201,8 +1275,8 @@ int plan_schedule(int tiles, int total, int bn, const SplitBuffers& sb, MainPara
     const int64_t len = static_cast<int64_t>(rem) * total;
     // never fewer CTAs than remaining tiles (that would be worse than whole tiles)
     const int ctas = static_cast<int>(std::min<int64_t>(sms, std::max<int64_t>(rem, len / kMinSkStages)));
-    const size_t need = static_cast<size_t>(2) * ctas * kTileP * bn * sizeof(float);
-    if (need <= sb.partial_bytes && rem <= sb.counter_cap) {
+    const size_t need = static_cast<size_t>(2) * ctas * per_unit * kTileP * bn * sizeof(float);
+    if (need <= sb.partial_bytes && rem * per_unit <= sb.counter_cap) {
       mp.dp_tiles = full * sms;
       mp.dp_rounds = full;
       mp.sk_tiles = rem;
@@ -1220,36 +1294,54 @@ int plan_schedule(int tiles, int total, int bn, const SplitBuffers& sb, MainPara
   return grid;
 }
 
-template <int BN, bool kTrans, bool kAbsTma>
+template <int BN, bool kTrans, bool kAbsTma, bool kPair>
 cudaError_t launch_main_bn(const CUtensorMap (&maps)[7], MainParams mp, int P, int M, const SplitBuffers& sb,
                            cudaStream_t stream) {
-  auto kern = lora_main_kernel<BN, kTrans, kAbsTma>;
-  cudaError_t e = set_smem(kern, MainSmem<BN>::kBytes);
+  using S = MainSmem<BN, kPair>;
+  auto kern = lora_main_kernel<BN, kTrans, kAbsTma, kPair>;
+  cudaError_t e = set_smem(kern, S::kBytes);
   if (e != cudaSuccess) return e;
-  mp.p_tiles = (P + kTileP - 1) / kTileP;
-  mp.t_tiles = (M + BN - 1) / BN;
-  const int grid = plan_schedule(mp.p_tiles * mp.t_tiles, mp.num_kt + mp.num_lt, BN, sb, mp);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(kMainThreads, 1, 1);
-  cfg.dynamicSmemBytes = MainSmem<BN>::kBytes;
+  cfg.dynamicSmemBytes = S::kBytes;
   cfg.stream = stream;
   // programmatic serialisation: the NF4 stages start while the low-rank kernel
   // before this one finishes; the producer waits for it before the LoRA stages
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kPair ? 2 : 1;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = kPair ? 2 : 1;
+  // units: one CTA per SM, or as many CTA pairs as can be resident at once
+  int units = sm_count();
+  if (kPair) {
+    static int pairs = 0;
+    if (pairs == 0) {
+      cfg.gridDim = dim3(2 * (units / 2), 1, 1);
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      pairs = std::max(1, std::min(n, units / 2));
+    }
+    units = pairs;
+  }
+  mp.p_tiles = (P + (kPair ? 2 * kTileP : kTileP) - 1) / (kPair ? 2 * kTileP : kTileP);
+  mp.t_tiles = (M + BN - 1) / BN;
+  const int grid = plan_schedule(mp.p_tiles * mp.t_tiles, mp.num_kt + mp.num_lt, BN, sb, mp, units, kPair ? 2 : 1);
+  cfg.gridDim = dim3(grid * (kPair ? 2 : 1), 1, 1);
   LaunchScope scope(kTrans ? kKindMainDx : kKindMainFwd, stream);
   return cudaLaunchKernelEx(&cfg, kern, maps[0], maps[1], maps[2], maps[3], maps[4], maps[5], maps[6], mp);
 }
 
-template <int BN, bool kTrans>
+template <int BN, bool kTrans, bool kPair = false>
 cudaError_t launch_main_abs(const CUtensorMap (&maps)[7], const MainParams& mp, bool abs_tma, int P,
                             int M, const SplitBuffers& sb, cudaStream_t stream) {
-  if (abs_tma) return launch_main_bn<BN, kTrans, true>(maps, mp, P, M, sb, stream);
-  return launch_main_bn<BN, kTrans, false>(maps, mp, P, M, sb, stream);
+  if (abs_tma) return launch_main_bn<BN, kTrans, true, kPair>(maps, mp, P, M, sb, stream);
+  return launch_main_bn<BN, kTrans, false, kPair>(maps, mp, P, M, sb, stream);
 }
 
 int pick_bn(int M) { return M <= 32 ? 32 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256)); }
@@ -1278,10 +1370,15 @@ cudaError_t launch_main(const LayerDims& d, const uint16_t* act, const uint16_t*
   const int C = kTrans ? d.N : d.K;     // contraction length of the NF4 part
   const int bn = pick_bn(d.M);
   const bool abs_tma = (d.K % 256) == 0;   // absmax rows are 16-byte multiples
+  // CTA pairs for the widest token tiles; the two CTAs of a pair share the
+  // low-rank contraction, so stacked projections need group ends on 256-row bounds
+  bool pair = bn == 256 && P >= 2 * kTileP;
+  if (!kTrans && d.groups.n > 0)
+    for (int g = 0; g < d.groups.n; ++g) pair = pair && d.groups.end[g] % (2 * kTileP) == 0;
   CUtensorMap maps[7];
   const bool gated = kTrans ? gate.dgu != nullptr : gate.h != nullptr;
   if (kTrans && gated) out = gate.dgu;   // dX is not stored; its map is never used
-  const int box_t = bn < 256 ? bn : 256;   // token rows per TMA box
+  const int box_t = pair ? bn / 2 : (bn < 256 ? bn : 256);   // token rows per TMA box
   bool ok = map_bf16(&maps[0], act, C, d.M, 64, box_t, true) && map_bf16(&maps[1], lact, d.rp, d.M, 64, box_t, true) &&
             make_map(&maps[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, P, d.M, static_cast<uint64_t>(P) * 2, 64,
                      kEpiChunk, true);
@@ -1326,6 +1423,7 @@ cudaError_t launch_main(const LayerDims& d, const uint16_t* act, const uint16_t*
   if (bn == 32) return launch_main_abs<32, kTrans>(maps, mp, abs_tma, P, d.M, sb, stream);
   if (bn == 64) return launch_main_abs<64, kTrans>(maps, mp, abs_tma, P, d.M, sb, stream);
   if (bn == 128) return launch_main_abs<128, kTrans>(maps, mp, abs_tma, P, d.M, sb, stream);
+  if (pair) return launch_main_abs<256, kTrans, true>(maps, mp, abs_tma, P, d.M, sb, stream);
   return launch_main_abs<256, kTrans>(maps, mp, abs_tma, P, d.M, sb, stream);
 }
 

@@ -197,6 +197,62 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t local_smem, uint32_t cta
   return r;
 }
 
+// Arrive on an mbarrier of any CTA of the cluster (address from map_to_cta).
+// Default semantics (release at CTA scope): the CTA-pair kernel uses it to
+// announce shared-memory data that TMA or this CTA's threads had completed
+// before this thread observed their local barrier; a cluster-scope release
+// measured about 0.6 us per arrival, longer than a pipeline stage.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Phase probes with cluster-scope acquire: for barriers that another CTA of
+// the cluster arrives on (or a CTA-pair tcgen05.commit signals).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+// mbar_wait with cluster-scope acquire; same limit and abort behaviour.
+static __device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity, Abort ab,
+                                                           bool honour_abort) {
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_cluster(bar, parity, 20000u)) return true;
+    if (honour_abort && *ab.flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *ab.flag = 1;
+      atomicExch(ab.status, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, Abort ab,
+                                                  bool honour_abort = true) {
+  if (mbar_test_wait_cluster(bar, parity)) return true;
+  return mbar_wait_cluster_slow(bar, parity, ab, honour_abort);
+}
+
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t cluster_addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
@@ -271,6 +327,21 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
+// CTA-pair forms: one warp of each CTA of the pair executes them together; the
+// same columns are allocated in both CTAs' TMEM and the address is written to
+// each CTA's own `dst`.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
 // 32 consecutive fp32 columns of this thread's TMEM lane (32x32b shape: warp w
 // of the CTA reads lanes 32*(w%4) .. 32*(w%4)+31).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
@@ -336,6 +407,30 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// CTA-pair UMMA, issued by one thread of the even CTA of the pair: M = 256
+// rows, A rows 0..127 from this CTA's shared memory and rows 128..255 from
+// the peer's (same offsets); B columns split the same way (N/2 from each);
+// D rows 0..127 in this CTA's TMEM, rows 128..255 in the peer's.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive (once) on the barrier at offset `bar` of every CTA of the pair in
+// `cta_mask` when this thread's previously issued pair UMMAs have completed.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          bar),
+      "h"(cta_mask)
       : "memory");
 }
 
