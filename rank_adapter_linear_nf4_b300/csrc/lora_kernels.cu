@@ -957,34 +957,50 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     auto store_chunk = [&](const float (&f)[32], int p0, int t0, int c0) {
       if (kTrans && p.gate) {
         // dX of the down layer of a SwiGLU block: dh never goes to memory; the
-        // gate's backward turns it, with g and u from gu, into dgu (layout of gu).
-        // dh is rounded to bf16 first, as the unfused block stores it.
-        const int n = p0 + prow;   // a feature of d_ff
-        if (n >= p.K) return;
+        // gate's backward turns it, with g and u read from gu, into dgu (layout
+        // of gu).  dh is rounded to bf16 first, as the unfused block stores it.
+        // Lanes pair up (shuffle): the even lane takes tokens 0..15 of the
+        // chunk and the odd lane tokens 16..31, each for both features of the
+        // pair, so every gu / dgu access is a 4-byte (bf16x2) one, and all 32
+        // loads of a lane are issued before the first is used.
+        const int n = p0 + f_even;   // the pair's first feature of d_ff
+        const bool feat_ok = n < p.K;
         const int64_t pitch = 2 * static_cast<int64_t>(p.K);
         const int64_t gcol = static_cast<int64_t>(n >> 6) * 128 + (n & 63);
+        const int tok0 = t0 + c0 + (odd ? 16 : 0);
+        float lo[16], hi[16];   // dh of features n and n + 1
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float gv[16], uv[16];
+        for (int q = 0; q < 16; ++q) {
+          const float mine = odd ? f[16 + q] : f[q];
+          const float got = __shfl_xor_sync(0xffffffffu, odd ? f[q] : f[16 + q], 1);
+          lo[q] = __bfloat162float(__float2bfloat16_rn(odd ? got : mine));
+          hi[q] = __bfloat162float(__float2bfloat16_rn(odd ? mine : got));
+        }
+        uint32_t gw[16], uw[16];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const int tok = t0 + c0 + 16 * half + q;
-            const int64_t at = static_cast<int64_t>(tok < p.M ? tok : 0) * pitch + gcol;
-            gv[q] = __bfloat162float(__ushort_as_bfloat16(__ldg(p.gu + at)));
-            uv[q] = __bfloat162float(__ushort_as_bfloat16(__ldg(p.gu + at + 64)));
+        for (int q = 0; q < 16; ++q) {
+          const int tok = tok0 + q;
+          const int64_t at = static_cast<int64_t>(tok < p.M ? tok : 0) * pitch + gcol;
+          gw[q] = feat_ok ? __ldg(reinterpret_cast<const unsigned int*>(p.gu + at)) : 0u;
+          uw[q] = feat_ok ? __ldg(reinterpret_cast<const unsigned int*>(p.gu + at + 64)) : 0u;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int tok = tok0 + q;
+          if (!feat_ok || tok >= p.M) continue;
+          float dg[2], du[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float gv = __uint_as_float(e ? (gw[q] & 0xFFFF0000u) : (gw[q] << 16));
+            const float uv = __uint_as_float(e ? (uw[q] & 0xFFFF0000u) : (uw[q] << 16));
+            const float dh = e ? hi[q] : lo[q];
+            const float sg = gate_sigmoid(gv);
+            du[e] = dh * gv * sg;
+            dg[e] = dh * uv * sg * (1.f + gv * (1.f - sg));
           }
-#pragma unroll
-          for (int q = 0; q < 16; ++q) {
-            const int tok = t0 + c0 + 16 * half + q;
-            if (tok >= p.M) continue;
-            const float dh = __bfloat162float(__float2bfloat16_rn(f[16 * half + q]));
-            const float sg = gate_sigmoid(gv[q]);
-            const float du = dh * gv[q] * sg;
-            const float dg = dh * uv[q] * sg * (1.f + gv[q] * (1.f - sg));
-            const int64_t at = static_cast<int64_t>(tok) * pitch + gcol;
-            p.dgu[at] = __bfloat16_as_ushort(__float2bfloat16_rn(dg));
-            p.dgu[at + 64] = __bfloat16_as_ushort(__float2bfloat16_rn(du));
-          }
+          const int64_t at = static_cast<int64_t>(tok) * pitch + gcol;
+          *reinterpret_cast<uint32_t*>(p.dgu + at) = pack_bf16x2(dg[0], dg[1]);
+          *reinterpret_cast<uint32_t*>(p.dgu + at + 64) = pack_bf16x2(du[0], du[1]);
         }
         return;
       }
