@@ -220,7 +220,7 @@ struct MergePSmem {
   static constexpr int kOpBytes = kChunks * 16384;            // one operand (B^T or an A^T tile)
   static constexpr int kBtOff = 0;
   static constexpr int kAOff = kBtOff + kOpBytes;
-  static constexpr int kStageOff = kAOff + kMpASlots * kOpBytes;   // two 32 KB output stagings
+  static constexpr int kStageOff = kAOff + kMpASlots * kOpBytes;   // 16 warps x two 2 KB output stagings
   static constexpr int kBarOff = kStageOff + 2 * 32768;
   // bars: a_full[2], a_empty[2], tmem_full[2], tmem_empty[2], bt_full, bt_free, drain
   static constexpr int kBytes = kBarOff + 8 * 11 + 1024;
@@ -228,7 +228,7 @@ struct MergePSmem {
 
 template <int RP>
 __global__ void __launch_bounds__(kMpThreads, 1)
-    lora_merge_persistent_kernel(const __grid_constant__ CUtensorMap map_out,   // W_out [N, K] bf16, box {64, 128}
+    lora_merge_persistent_kernel(const __grid_constant__ CUtensorMap map_out,   // W_out [N, K] bf16, box {32, 32}, 64-B swizzle
                                  const __grid_constant__ CUtensorMap map_a,     // A [K, r] bf16, box {64, 128}, SW128
                                  const __grid_constant__ CUtensorMap map_b,     // B [r, N] bf16, box {64, 64}, SW128
                                  const MergeParams p, int k_tiles, int tiles) {
@@ -350,6 +350,9 @@ __global__ void __launch_bounds__(kMpThreads, 1)
     // ---------------- epilogue: row i of the tile, columns 32*q .. 32*q+31
     const int quarter = warp & 3, q = warp >> 2;
     const int i = quarter * 32 + lane;
+    // each warp stores its own 32 x 32 box (its TMEM rows, its 32 columns)
+    // from two 2 KB stagings of its own, so no barrier spans the warps
+    const uint32_t my_stage = base + S::kStageOff + static_cast<uint32_t>(warp) * 4096u;
     const int kblocks = p.K >> 6;
     // codes (16 B) and absmax of tile `tile` for this thread, zero outside the matrix
     auto fetch = [&](int tile, uint4& c, float& am) {
@@ -369,8 +372,7 @@ __global__ void __launch_bounds__(kMpThreads, 1)
     for (int it = 0, tile = t_begin; tile < t_end; ++it, ++tile) {
       const int buf = it & 1;
       fetch(tile + 2, c2, a2);
-      // every epilogue warp runs every iteration and meets both named barriers,
-      // whether or not a wait ran out (then it only skips the work)
+      // a warp whose wait ran out only skips the work
       const bool ok = __all_sync(0xffffffffu, mbar_wait(tmem_full(buf), (it >> 1) & 1, ab));
       uint32_t v[32];
       if (ok) {
@@ -381,15 +383,14 @@ __global__ void __launch_bounds__(kMpThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(tmem_empty(buf));
       }
-      // the staging buffer of this tile was last stored two tiles ago
-      if (threadIdx.x == 0) tma_store_wait_read_le1();
-      named_bar_sync(1, kMpEpiWarps * 32);
+      // this warp's staging `buf` was last stored two tiles ago
+      if (lane == 0) tma_store_wait_read_le1();
+      __syncwarp();
       if (ok) {
         const Nf4BlockTable tab = nf4_block_table(a0);
         const uint32_t words[4] = {c0.x, c0.y, c0.z, c0.w};
-        // staging: two [128 rows][64 columns] halves, 128-byte swizzled rows
-        const uint32_t row = base + S::kStageOff + buf * 32768u + static_cast<uint32_t>(q >> 1) * 16384u +
-                             static_cast<uint32_t>(i) * 128u;
+        // staging: this warp's [32 rows][32 columns], 64-byte rows, 64-byte swizzle
+        const uint32_t row = my_stage + static_cast<uint32_t>(buf) * 2048u + static_cast<uint32_t>(lane) * 64u;
 #pragma unroll
         for (int wq = 0; wq < 4; ++wq) {
           const uint4 wd = nf4_expand8(words[wq], tab);   // elements 8wq..8wq+7 of the thread's 32
@@ -401,24 +402,26 @@ __global__ void __launch_bounds__(kMpThreads, 1)
             o[e] = pack_bf16x2(fmaf(p.s, __uint_as_float(v[8 * wq + 2 * e]), w0),
                                fmaf(p.s, __uint_as_float(v[8 * wq + 2 * e + 1]), w1));
           }
-          const uint32_t chunk = static_cast<uint32_t>((q & 1) * 4 + wq);   // 16-B chunk of the 128-B row
-          st_shared_v4(row + ((chunk ^ static_cast<uint32_t>(i & 7)) << 4), make_uint4(o[0], o[1], o[2], o[3]));
+          const uint32_t chunk = static_cast<uint32_t>(wq) ^ (static_cast<uint32_t>(lane >> 1) & 3u);
+          st_shared_v4(row + (chunk << 4), make_uint4(o[0], o[1], o[2], o[3]));
         }
         fence_proxy_async_smem();
       }
-      named_bar_sync(1, kMpEpiWarps * 32);
-      if (threadIdx.x == 0 && s_abort == 0) {
-        const int n0 = (tile / k_tiles) * kMergeTile, k0 = (tile % k_tiles) * kMergeTile;
-        tma_store_2d(&map_out, base + S::kStageOff + buf * 32768u, k0, n0);
-        if (k0 + 64 < p.K) tma_store_2d(&map_out, base + S::kStageOff + buf * 32768u + 16384u, k0 + 64, n0);
-        tma_store_commit();
+      __syncwarp();
+      if (lane == 0 && ok) {
+        // boxes wholly outside the matrix are not stored
+        const int nr = (tile / k_tiles) * kMergeTile + quarter * 32, kc = (tile % k_tiles) * kMergeTile + 32 * q;
+        if (nr < p.N && kc < p.K) {
+          tma_store_2d(&map_out, my_stage + static_cast<uint32_t>(buf) * 2048u, kc, nr);
+          tma_store_commit();
+        }
       }
       c0 = c1;
       a0 = a1;
       c1 = c2;
       a1 = a2;
     }
-    if (threadIdx.x == 0) tma_store_wait_all();
+    if (lane == 0) tma_store_wait_all();
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -479,8 +482,10 @@ cudaError_t launch_merge_nf4(const uint8_t* packed, const float* absmax, int N, 
   if (mp.a_vec && mp.b_vec) {
     // A^T and B^T tiles by TMA: rows of A are r * 2 bytes (a multiple of 16 when r % 8 == 0)
     CUtensorMap maps[3];
-    maps[0] = map_out;
-    if (!make_tensor_map_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, static_cast<uint64_t>(r),
+    if (!make_tensor_map_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, static_cast<uint64_t>(K),
+                            static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, 32, 32,
+                            CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_tensor_map_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, static_cast<uint64_t>(r),
                             static_cast<uint64_t>(K), static_cast<uint64_t>(r) * 2, 64, kMergeTile,
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, B, static_cast<uint64_t>(N),
