@@ -146,9 +146,13 @@ __device__ __forceinline__ uint32_t quantize_group(const uint4 v, uint32_t tab_l
     const uint32_t k = __float_as_uint(__fmaf_rn(x[i], 64.0f, kBinMagic)) & 0xFFu;
     uint32_t tq0, tq1;
     asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(tq0), "=r"(tq1) : "r"(tab_lane + k * 128u));
-    const uint32_t q = tq1 + (x[i] >= __uint_as_float(tq0) ? 1u : 0u);
+    // x >= t as an all-ones mask (false for NaN), so q = q_base - mask
+    uint32_t ge;
+    asm("set.ge.u32.f32 %0, %1, %2;" : "=r"(ge) : "f"(x[i]), "f"(__uint_as_float(tq0)));
+    const uint32_t q = tq1 - ge;
     // byte b holds code 2b in its high nibble and code 2b+1 in its low nibble
-    word |= q << (8 * (i >> 1) + ((i & 1) ? 0 : 4));
+    // (the nibbles do not overlap: adding is or-ing)
+    word += q << (8 * (i >> 1) + ((i & 1) ? 0 : 4));
   }
   return word;
 }
