@@ -110,7 +110,6 @@ QuantTable make_quant_table(const Thresholds& th, bool* ok) {
 constexpr int kQuantThreads = 256;
 constexpr int kQuantGroupsPerThread = 2;
 constexpr int kQuantChunk = kQuantThreads * kQuantGroupsPerThread;   // groups per chunk
-constexpr int kQuantCtasPerSm = 6;
 
 // The 8 codes of one group (one bf16 word quadruple), packed two per byte
 // (first element in the high nibble), and the block absmax.
@@ -300,7 +299,15 @@ cudaError_t launch_quantize_nf4(const uint16_t* W, int64_t n_elems, uint8_t* pac
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  const int64_t grid = std::min<int64_t>(chunks, static_cast<int64_t>(sms) * kQuantCtasPerSm);
+  // persistent: exactly the CTAs that can be resident at once (registers, not
+  // the 32 KB table, limit them), so that no CTA starts after another has finished
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nf4_quantize_kernel, kQuantThreads, 0);
+    if (e != cudaSuccess) return e;
+    per_sm = std::max(per_sm, 1);
+  }
+  const int64_t grid = std::min<int64_t>(chunks, static_cast<int64_t>(sms) * per_sm);
   LaunchScope scope(kKindQuantize, stream);
   nf4_quantize_kernel<<<static_cast<unsigned>(grid), kQuantThreads, 0, stream>>>(
       reinterpret_cast<const uint4*>(W), n_groups, reinterpret_cast<uint32_t*>(packed), absmax, table);
