@@ -1335,14 +1335,15 @@ cudaError_t launch_main_bn(const CUtensorMap (&maps)[7], MainParams mp, int P, i
   // units: one CTA per SM, or as many CTA pairs as can be resident at once
   int units = sm_count();
   if (kPair) {
-    static int pairs = 0;
-    if (pairs == 0) {
-      cfg.gridDim = dim3(2 * (units / 2), 1, 1);
+    // queried once (thread-safe initialisation); 0 if the query failed
+    static const int pairs = [&]() {
+      cudaLaunchConfig_t q = cfg;
+      q.gridDim = dim3(2 * (units / 2), 1, 1);
       int n = 0;
-      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
-      if (e != cudaSuccess) return e;
-      pairs = std::max(1, std::min(n, units / 2));
-    }
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess) return 0;
+      return std::max(1, std::min(n, units / 2));
+    }();
+    if (pairs == 0) return cudaErrorInvalidConfiguration;
     units = pairs;
   }
   mp.p_tiles = (P + (kPair ? 2 * kTileP : kTileP) - 1) / (kPair ? 2 * kTileP : kTileP);

@@ -276,7 +276,13 @@ cudaError_t launch_quantize_absmax_dq(const float* absmax, int64_t n, uint8_t* q
 
 cudaError_t launch_dequant_absmax_dq(const uint8_t* q8, const float* scale2, int64_t n, float* absmax,
                                      cudaStream_t stream) {
-  const int64_t grid = std::min<int64_t>((n + 255) / 256, 148 * 8);
+  // grid-stride: at most the CTAs that can be resident at once
+  int dev = 0, sms = 148, per_sm = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, absmax_dq_dequant_kernel, 256, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t grid = std::min<int64_t>((n + 255) / 256, static_cast<int64_t>(sms) * per_sm);
   LaunchScope scope(kKindAbsmaxDq, stream);
   absmax_dq_dequant_kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(q8, scale2, n, absmax);
   return cudaGetLastError();
@@ -301,12 +307,12 @@ cudaError_t launch_quantize_nf4(const uint16_t* W, int64_t n_elems, uint8_t* pac
   if (e != cudaSuccess) return e;
   // persistent: exactly the CTAs that can be resident at once (registers, not
   // the 32 KB table, limit them), so that no CTA starts after another has finished
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, nf4_quantize_kernel, kQuantThreads, 0);
-    if (e != cudaSuccess) return e;
-    per_sm = std::max(per_sm, 1);
-  }
+  static const int per_sm = [] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, nf4_quantize_kernel, kQuantThreads, 0) != cudaSuccess)
+      return 1;
+    return std::max(n, 1);
+  }();
   const int64_t grid = std::min<int64_t>(chunks, static_cast<int64_t>(sms) * per_sm);
   LaunchScope scope(kKindQuantize, stream);
   nf4_quantize_kernel<<<static_cast<unsigned>(grid), kQuantThreads, 0, stream>>>(

@@ -98,11 +98,16 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(const uint16_t* __restr
   }
 }
 
-int swiglu_grid(int64_t rows, int64_t d_ff) {
-  int dev = 0, sms = 148;
+// Grid-stride kernels: at most the CTAs of 256 threads that can be resident
+// at once (a CTA that starts only after another has finished would run its
+// share at the end, alone).
+template <typename Kern>
+int swiglu_grid(Kern kern, int64_t rows, int64_t d_ff) {
+  int dev = 0, sms = 148, per_sm = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess || per_sm < 1) per_sm = 1;
   const int64_t want = (rows * (d_ff / 8) + 255) / 256;
-  const int64_t cap = static_cast<int64_t>(sms) * 8;   // 8 CTAs of 256 threads per SM, grid-stride beyond
+  const int64_t cap = static_cast<int64_t>(sms) * per_sm;
   return static_cast<int>(want < cap ? want : cap);
 }
 
@@ -112,7 +117,7 @@ cudaError_t launch_swiglu_fwd(const uint16_t* gu, int64_t rows, int64_t d_ff, ui
                               cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   LaunchScope scope(kKindSwigluFwd, stream);
-  swiglu_fwd_kernel<<<swiglu_grid(rows, d_ff), 256, 0, stream>>>(gu, rows, d_ff, h, interleaved);
+  swiglu_fwd_kernel<<<swiglu_grid(swiglu_fwd_kernel, rows, d_ff), 256, 0, stream>>>(gu, rows, d_ff, h, interleaved);
   return cudaGetLastError();
 }
 
@@ -120,7 +125,7 @@ cudaError_t launch_swiglu_bwd(const uint16_t* gu, const uint16_t* dh, int64_t ro
                               bool interleaved, cudaStream_t stream) {
   if (rows == 0) return cudaSuccess;
   LaunchScope scope(kKindSwigluBwd, stream);
-  swiglu_bwd_kernel<<<swiglu_grid(rows, d_ff), 256, 0, stream>>>(gu, dh, rows, d_ff, dgu, interleaved);
+  swiglu_bwd_kernel<<<swiglu_grid(swiglu_bwd_kernel, rows, d_ff), 256, 0, stream>>>(gu, dh, rows, d_ff, dgu, interleaved);
   return cudaGetLastError();
 }
 
