@@ -739,40 +739,83 @@ def run_ours(args):
 
 def e2e_timing(wl, args, timed, flops, world):
     """Forward + backward through the public API from pinned host inputs to host
-    outputs, the copies inside the timed region."""
+    outputs, the copies inside the timed region, pipelined as a caller streaming
+    host data would: two sets of device buffers, uploads on one stream and
+    downloads on another, so that step i+1's upload and step i-1's download run
+    beside step i's kernels (and beside each other: the link carries both
+    directions at once).  Every step still uploads its X and dY and reads back
+    its Y, dX, dA and dB."""
     import torch
     from rank_adapter_linear_nf4_b300 import qlora
     sh, t0 = wl.sh, wl.sets[0]
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     hX = t0["X"].cpu().pin_memory()
     hdY = None if wl.only_fwd else wl.dY0.cpu().pin_memory()
-    hY = torch.empty_like(t0["Y"], device="cpu").pin_memory()
-    hdX = None if wl.only_fwd else torch.empty_like(t0["dX"], device="cpu").pin_memory()
-    hdA = torch.empty_like(t0["dA"], device="cpu").pin_memory()
-    hdB = torch.empty_like(t0["dB"], device="cpu").pin_memory()
-    X_in = torch.empty_like(t0["X"])
-    dY_in = None if wl.only_fwd else torch.empty_like(wl.dY0)
+    sets = []
+    for _ in range(2):
+        d = {"X": torch.empty_like(t0["X"]), "Y": torch.empty_like(t0["Y"]), "XA": torch.empty_like(t0["XA"]),
+             "hY": torch.empty_like(t0["Y"], device="cpu").pin_memory()}
+        for k in ("x_ready", "dy_ready", "fwd_done", "bwd_done", "out_done"):
+            d[k] = torch.cuda.Event()
+        if not wl.only_fwd:
+            d.update({"dY": torch.empty_like(wl.dY0), "dX": torch.empty_like(t0["dX"]),
+                      "dA": torch.empty_like(t0["dA"]), "dB": torch.empty_like(t0["dB"]),
+                      "hdX": torch.empty_like(t0["dX"], device="cpu").pin_memory(),
+                      "hdA": torch.empty_like(t0["dA"], device="cpu").pin_memory(),
+                      "hdB": torch.empty_like(t0["dB"], device="cpu").pin_memory()})
+        sets.append(d)
+    steps = max(3, min(args.steps, 200))
 
     def e2e_step(i):
-        X_in.copy_(hX, non_blocking=True)
+        d = sets[i % 2]
+        if i == 0:
+            s_in.wait_stream(comp)   # nothing before the region's start
+        # upload: this set's inputs were last read by step i-2's kernels
+        if i >= 2:
+            s_in.wait_event(d["bwd_done"])
+        with torch.cuda.stream(s_in):
+            d["X"].copy_(hX, non_blocking=True)
+            d["x_ready"].record(s_in)
+            if not wl.only_fwd:
+                d["dY"].copy_(hdY, non_blocking=True)
+                d["dy_ready"].record(s_in)
+        # kernels: this set's outputs were last read back by step i-2's download
+        comp.wait_event(d["x_ready"])
+        if i >= 2:
+            comp.wait_event(d["out_done"])
+        qlora.qlora_linear_fwd(d["X"], t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
+                               Y=d["Y"], XA=d["XA"], workspace=wl.ws)
+        d["fwd_done"].record(comp)
         if not wl.only_fwd:
-            dY_in.copy_(hdY, non_blocking=True)
-        qlora.qlora_linear_fwd(X_in, t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
-                               Y=t0["Y"], XA=t0["XA"], workspace=wl.ws)
-        hY.copy_(t0["Y"], non_blocking=True)
-        if not wl.only_fwd:
-            qlora.qlora_linear_bwd(X_in, dY_in, t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
-                                   t0["XA"], dX=t0["dX"], dA=t0["dA"], dB=t0["dB"], workspace=wl.ws)
-            hdX.copy_(t0["dX"], non_blocking=True)
-            hdA.copy_(t0["dA"], non_blocking=True)
-            hdB.copy_(t0["dB"], non_blocking=True)
+            comp.wait_event(d["dy_ready"])
+            qlora.qlora_linear_bwd(d["X"], d["dY"], t0["packed"], t0["absmax"], t0["A"], t0["B"], sh.s,
+                                   d["XA"], dX=d["dX"], dA=d["dA"], dB=d["dB"], workspace=wl.ws)
+        d["bwd_done"].record(comp)
+        # download: Y as soon as the forward is done, the gradients after the backward
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(d["fwd_done"])
+            d["hY"].copy_(d["Y"], non_blocking=True)
+            if not wl.only_fwd:
+                s_out.wait_event(d["bwd_done"])
+                d["hdX"].copy_(d["dX"], non_blocking=True)
+                d["hdA"].copy_(d["dA"], non_blocking=True)
+                d["hdB"].copy_(d["dB"], non_blocking=True)
+            d["out_done"].record(s_out)
+        if i == steps - 1:
+            comp.wait_stream(s_out)   # the region ends after the last download
+            comp.wait_stream(s_in)
 
-    e2e_step(0)
-    steps = max(3, min(args.steps, 200))
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
     ms = timed(e2e_step, steps)[0] / steps
     h2d = hX.numel() * 2 + (0 if wl.only_fwd else hdY.numel() * 2)
-    d2h = hY.numel() * 2 + (0 if wl.only_fwd else hdX.numel() * 2 + hdA.numel() * 4 + hdB.numel() * 4)
+    d2h = t0["Y"].numel() * 2 + (0 if wl.only_fwd else t0["dX"].numel() * 2 + t0["dA"].numel() * 4 +
+                                 t0["dB"].numel() * 4)
     return {"value": flops * world / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms, "steps": steps,
+            "pipeline": "two buffer sets; uploads and downloads on their own streams",
             "l2_note": wl.l2_note()}
 
 
