@@ -824,13 +824,21 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           const bool two = (s + 1 < se) && mbar_test_wait(full(slot2), fpar2) &&
                            (!kPair || mbar_test_wait_cluster(pfull(slot2), fpar2));
           tc_fence_after_sync();
-          issue_stage(tmem_d, slot, s >= p.num_kt, s == sb);
-          if (two) issue_stage(tmem_d, slot2, s + 1 >= p.num_kt, false);
-          // a pair's commit frees the stage in both CTAs
           if (kPair) {
+            // each stage's commit right behind its own MMAs (a commit completes
+            // when all of this thread's earlier MMAs have: committing after the
+            // second stage's MMAs frees the first a stage late); the commit
+            // frees the stage in both CTAs of the pair.  Measured faster for
+            // the pair's deeper ring, slower for the one-CTA form at short stages.
+            issue_stage(tmem_d, slot, s >= p.num_kt, s == sb);
             umma_commit_pair(empty(slot), 3);
-            if (two) umma_commit_pair(empty(slot2), 3);
+            if (two) {
+              issue_stage(tmem_d, slot2, s + 1 >= p.num_kt, false);
+              umma_commit_pair(empty(slot2), 3);
+            }
           } else {
+            issue_stage(tmem_d, slot, s >= p.num_kt, s == sb);
+            if (two) issue_stage(tmem_d, slot2, s + 1 >= p.num_kt, false);
             umma_commit(empty(slot));
             if (two) umma_commit(empty(slot2));
           }
