@@ -305,15 +305,21 @@ class OracleRunner:
     """The oracle on the first `tokens` tokens of the workload: one step is
     NF4 dequantisation of the full weight + forward + backward (fp64)."""
 
+    # quantised weights by (d_in, d_out, r): workloads of one weight shape share one
+    _weights = {}
+
     def __init__(self, sh, tokens: int):
         from oracle import qlora_oracle as O
         from rank_adapter_linear_nf4_b300 import synthetic
         self.O, self.sh = O, sh
         X, dY = synthetic.activations(tokens, sh.d_in, sh.d_out, seed=0)
-        W, A, B = synthetic.weights(sh.d_in, sh.d_out, sh.r, seed=1)
         f = lambda t: t.float().numpy()
-        self.X, self.dY, self.A, self.B = f(X), f(dY), f(A), f(B)
-        self.packed, self.absmax = O.quantize_nf4(f(W))
+        self.X, self.dY = f(X), f(dY)
+        key = (sh.d_in, sh.d_out, sh.r)
+        if key not in OracleRunner._weights:
+            W, A, B = synthetic.weights(sh.d_in, sh.d_out, sh.r, seed=1)
+            OracleRunner._weights[key] = (f(A), f(B)) + tuple(O.quantize_nf4(f(W)))
+        self.A, self.B, self.packed, self.absmax = OracleRunner._weights[key]
         self.fwd_only = fwd_only(sh)
 
     @staticmethod
@@ -362,6 +368,26 @@ def cpu_baseline(sh, min_seconds=10.0):
                      f"weight + fp64 forward{'' if fwd_only(sh) else ' + backward'}), median of {calls} calls, "
                      f"{per_call * 1e3:.1f} ms per call, {threads} BLAS threads"}
     out["single_thread"] = single_thread_baseline(sh, min_seconds / 2)
+    out["full_runs"] = cpu_full_runs()
+    return out
+
+
+# Workloads small enough for the oracle to run whole (every token) in seconds.
+CPU_FULL_CONFIGS = ("tiny", "sweep_m1", "sweep_m16", "sweep_m128")
+
+
+def cpu_full_runs(min_seconds=1.5):
+    """The oracle on whole small workloads, all BLAS threads: per workload the
+    median time of one step (NF4 dequantise of the full weight + fp64 forward,
+    and backward from 128 tokens on) and its rate."""
+    out = {}
+    for name in CPU_FULL_CONFIGS:
+        sh = shape_of(name)
+        runner = OracleRunner(sh, sh.M)
+        per_call, calls = runner.time_calls(min_seconds)
+        out[name] = {"ms_per_step": per_call * 1e3, "value": step_flops(sh) / per_call / 1e12, "unit": "TFLOP/s",
+                     "tokens_per_s": sh.M / per_call, "calls": calls,
+                     "step": "fwd" if fwd_only(sh) else "fwd+bwd"}
     return out
 
 
