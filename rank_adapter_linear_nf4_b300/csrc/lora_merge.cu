@@ -220,15 +220,17 @@ struct MergePSmem {
   static constexpr int kOpBytes = kChunks * 16384;            // one operand (B^T or an A^T tile)
   static constexpr int kBtOff = 0;
   static constexpr int kAOff = kBtOff + kOpBytes;
-  static constexpr int kStageOff = kAOff + kMpASlots * kOpBytes;   // 16 warps x two 2 KB output stagings
-  static constexpr int kBarOff = kStageOff + 2 * 32768;
+  static constexpr int kStageOff = kAOff + kMpASlots * kOpBytes;   // 16 warps x two 4 KB output stagings
+  static constexpr int kBarOff = kStageOff + kMpEpiWarps * 8192;
   // bars: a_full[2], a_empty[2], tmem_full[2], tmem_empty[2], bt_full, bt_free, drain
   static constexpr int kBytes = kBarOff + 8 * 11 + 1024;
+  static_assert(kBytes <= 232448, "shared memory budget");
+  static_assert(kStageOff % 1024 == 0, "stagings keep the 128-byte swizzle alignment");
 };
 
 template <int RP>
 __global__ void __launch_bounds__(kMpThreads, 1)
-    lora_merge_persistent_kernel(const __grid_constant__ CUtensorMap map_out,   // W_out [N, K] bf16, box {32, 32}, 64-B swizzle
+    lora_merge_persistent_kernel(const __grid_constant__ CUtensorMap map_out,   // W_out [N, K] bf16, box {64, 32}, 128-B swizzle
                                  const __grid_constant__ CUtensorMap map_a,     // A [K, r] bf16, box {64, 128}, SW128
                                  const __grid_constant__ CUtensorMap map_b,     // B [r, N] bf16, box {64, 64}, SW128
                                  const MergeParams p, int k_tiles, int tiles) {
@@ -257,7 +259,7 @@ __global__ void __launch_bounds__(kMpThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tmem_full(b), 1);
-      mbar_init(tmem_empty(b), kMpEpiWarps);
+      mbar_init(tmem_empty(b), kMpEpiWarps / 2);   // the half of the epilogue warps that finishes it
     }
     mbar_init(bt_full, 1);
     mbar_init(bt_free, 1);
@@ -347,78 +349,92 @@ __global__ void __launch_bounds__(kMpThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- epilogue: row i of the tile, columns 32*q .. 32*q+31
-    const int quarter = warp & 3, q = warp >> 2;
+    // ---------------- epilogue: warps 0-7 finish the CTA's even tiles (accumulator 0),
+    // warps 8-15 its odd ones (accumulator 1); in each half, thread (quarter, q)
+    // takes row i of the tile, columns 64*q .. 64*q+63: one whole NF4 block, so
+    // one block table serves 64 elements
+    const int half = warp >> 3, hw = warp & 7;
+    const int quarter = hw & 3, q = hw >> 2;
     const int i = quarter * 32 + lane;
-    // each warp stores its own 32 x 32 box (its TMEM rows, its 32 columns)
-    // from two 2 KB stagings of its own, so no barrier spans the warps
-    const uint32_t my_stage = base + S::kStageOff + static_cast<uint32_t>(warp) * 4096u;
+    // each warp stores its own 32 x 64 box (its TMEM rows, its 64 columns)
+    // from two 4 KB stagings of its own, so no barrier spans the warps
+    const uint32_t my_stage = base + S::kStageOff + static_cast<uint32_t>(warp) * 8192u;
     const int kblocks = p.K >> 6;
-    // codes (16 B) and absmax of tile `tile` for this thread, zero outside the matrix
-    auto fetch = [&](int tile, uint4& c, float& am) {
-      c = make_uint4(0u, 0u, 0u, 0u);
+    // codes (32 B) and absmax of tile `tile` for this thread, zero outside the matrix
+    auto fetch = [&](int tile, uint4& ca, uint4& cb, float& am) {
+      ca = make_uint4(0u, 0u, 0u, 0u);
+      cb = ca;
       am = 0.0f;
       if (tile >= t_end) return;
-      const int n = (tile / k_tiles) * kMergeTile + i, k = (tile % k_tiles) * kMergeTile + 32 * q;
+      const int n = (tile / k_tiles) * kMergeTile + i, k = (tile % k_tiles) * kMergeTile + 64 * q;
       if (n >= p.N || k >= p.K) return;
-      c = ldg_nc_v4(p.packed + static_cast<int64_t>(n) * (p.K / 2) + k / 2);
+      const uint8_t* src = p.packed + static_cast<int64_t>(n) * (p.K / 2) + k / 2;
+      ca = ldg_nc_v4(src);
+      cb = ldg_nc_v4(src + 16);
       am = ldg_nc_f32(p.absmax + static_cast<int64_t>(n) * kblocks + (k >> 6));
     };
-    // two tiles ahead
-    uint4 c0, c1, c2;
+    // this half's tiles are t_begin + half, + 2, ...; the next two are fetched ahead
+    uint4 c0a, c0b, c1a, c1b, c2a, c2b;
     float a0, a1, a2;
-    fetch(t_begin, c0, a0);
-    fetch(t_begin + 1, c1, a1);
-    for (int it = 0, tile = t_begin; tile < t_end; ++it, ++tile) {
-      const int buf = it & 1;
-      fetch(tile + 2, c2, a2);
+    fetch(t_begin + half, c0a, c0b, a0);
+    fetch(t_begin + half + 2, c1a, c1b, a1);
+    for (int j = 0, tile = t_begin + half; tile < t_end; ++j, tile += 2) {
+      fetch(tile + 4, c2a, c2b, a2);
       // a warp whose wait ran out only skips the work
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(tmem_full(buf), (it >> 1) & 1, ab));
-      uint32_t v[32];
-      if (ok) {
-        tc_fence_after_sync();
-        tmem_ld32(tmem + (static_cast<uint32_t>(quarter * 32) << 16) + buf * kMergeTile + 32 * q, v);
-        tmem_ld_wait();
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tmem_empty(buf));
-      }
-      // this warp's staging `buf` was last stored two tiles ago
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(tmem_full(half), j & 1, ab));
+      const int sb = j & 1;   // this warp's staging, last stored two of its tiles ago
       if (lane == 0) tma_store_wait_read_le1();
       __syncwarp();
       if (ok) {
+        tc_fence_after_sync();
         const Nf4BlockTable tab = nf4_block_table(a0);
-        const uint32_t words[4] = {c0.x, c0.y, c0.z, c0.w};
-        // staging: this warp's [32 rows][32 columns], 64-byte rows, 64-byte swizzle
-        const uint32_t row = my_stage + static_cast<uint32_t>(buf) * 2048u + static_cast<uint32_t>(lane) * 64u;
+        const uint32_t words[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
+        // staging: this warp's [32 rows][64 columns], 128-byte rows, 128-byte swizzle
+        const uint32_t row = my_stage + static_cast<uint32_t>(sb) * 4096u + static_cast<uint32_t>(lane) * 128u;
+        const uint32_t tacc = tmem + (static_cast<uint32_t>(quarter * 32) << 16) +
+                              static_cast<uint32_t>(half * kMergeTile + 64 * q);
 #pragma unroll
-        for (int wq = 0; wq < 4; ++wq) {
-          const uint4 wd = nf4_expand8(words[wq], tab);   // elements 8wq..8wq+7 of the thread's 32
-          const uint32_t pr[4] = {wd.x, wd.y, wd.z, wd.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float w0 = __uint_as_float(pr[e] << 16), w1 = __uint_as_float(pr[e] & 0xFFFF0000u);
-            o[e] = pack_bf16x2(fmaf(p.s, __uint_as_float(v[8 * wq + 2 * e]), w0),
-                               fmaf(p.s, __uint_as_float(v[8 * wq + 2 * e + 1]), w1));
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[32];
+          tmem_ld32(tacc + 32u * hh, v);
+          tmem_ld_wait();
+          if (hh == 1) {
+            // both column halves are in registers: the accumulator may be overwritten
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tmem_empty(half));
           }
-          const uint32_t chunk = static_cast<uint32_t>(wq) ^ (static_cast<uint32_t>(lane >> 1) & 3u);
-          st_shared_v4(row + (chunk << 4), make_uint4(o[0], o[1], o[2], o[3]));
+#pragma unroll
+          for (int wq = 0; wq < 4; ++wq) {
+            const uint4 wd = nf4_expand8(words[4 * hh + wq], tab);   // elements 32hh + 8wq .. +7 of the block
+            const uint32_t pr[4] = {wd.x, wd.y, wd.z, wd.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float w0 = __uint_as_float(pr[e] << 16), w1 = __uint_as_float(pr[e] & 0xFFFF0000u);
+              o[e] = pack_bf16x2(fmaf(p.s, __uint_as_float(v[8 * wq + 2 * e]), w0),
+                                 fmaf(p.s, __uint_as_float(v[8 * wq + 2 * e + 1]), w1));
+            }
+            const uint32_t chunk = static_cast<uint32_t>(4 * hh + wq) ^ (static_cast<uint32_t>(lane) & 7u);
+            st_shared_v4(row + (chunk << 4), make_uint4(o[0], o[1], o[2], o[3]));
+          }
         }
         fence_proxy_async_smem();
       }
       __syncwarp();
       if (lane == 0 && ok) {
         // boxes wholly outside the matrix are not stored
-        const int nr = (tile / k_tiles) * kMergeTile + quarter * 32, kc = (tile % k_tiles) * kMergeTile + 32 * q;
+        const int nr = (tile / k_tiles) * kMergeTile + quarter * 32, kc = (tile % k_tiles) * kMergeTile + 64 * q;
         if (nr < p.N && kc < p.K) {
-          tma_store_2d(&map_out, my_stage + static_cast<uint32_t>(buf) * 2048u, kc, nr);
+          tma_store_2d(&map_out, my_stage + static_cast<uint32_t>(sb) * 4096u, kc, nr);
           tma_store_commit();
         }
       }
-      c0 = c1;
+      c0a = c1a;
+      c0b = c1b;
       a0 = a1;
-      c1 = c2;
+      c1a = c2a;
+      c1b = c2b;
       a1 = a2;
     }
     if (lane == 0) tma_store_wait_all();
@@ -483,8 +499,8 @@ cudaError_t launch_merge_nf4(const uint8_t* packed, const float* absmax, int N, 
     // A^T and B^T tiles by TMA: rows of A are r * 2 bytes (a multiple of 16 when r % 8 == 0)
     CUtensorMap maps[3];
     if (!make_tensor_map_2d(&maps[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, out, static_cast<uint64_t>(K),
-                            static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, 32, 32,
-                            CU_TENSOR_MAP_SWIZZLE_64B) ||
+                            static_cast<uint64_t>(N), static_cast<uint64_t>(K) * 2, 64, 32,
+                            CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map_2d(&maps[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, A, static_cast<uint64_t>(r),
                             static_cast<uint64_t>(K), static_cast<uint64_t>(r) * 2, 64, kMergeTile,
                             CU_TENSOR_MAP_SWIZZLE_128B) ||
